@@ -1,0 +1,140 @@
+"""Seeded synthetic inputs for the dynamic short convolution.
+
+This module holds no arithmetic of the method itself: it only draws random
+tensors (torch CPU generator) and packed-document offsets.  The CUDA path's
+tests, the fp64 oracle's tests and the benchmark all take their inputs from
+here, so both sides see bit-identical data.
+
+Workloads (shapes follow the QKV placement of the notes on "Dynamic Short
+Convolutions Improve Transformers", section "Placement", at about 2B-model
+width; the pages benchmark no public suite, so these synthetic draws stand in
+for real activations):
+
+* ``tiny_fp32``     B=1 T=128  D=64   W=4 H=1   fp32; x~N(0,1), w~N(0,0.25) (std 0.5)
+* ``headwise_bf16`` B=8 T=2048 D=2048 W=4 H=16  bf16; x~N(0,1), w=0.1*N(0,1) + 0.5 on tap k=0
+* ``material_bf16`` B=4 T=4096 D=2048 W=4 H=1   bf16; w~N(0,0.1) (std sqrt(0.1))
+* ``lowrank_bf16``  B=8 T=2048 D=2048 W=4 R=64  bf16; z,x~N(0,1), U~N(0,1/R), bias~N(0,0.01) fp32
+* ``qkv_packed_bf16`` B=4 T=8192 D=3072 W=4 H=16 bf16 over packed documents with
+  lengths ~U{128..4096} per sequence (the last one truncated to fill T);
+  w~N(0,0.1)
+
+Upstream gradients dy ~ N(0,1) everywhere.  N(0, s) means variance s.
+Values are drawn in fp32 and rounded to nearest-even bf16 where the workload
+is bf16.  Seeds: 1000 * workload id + tensor index (x=0, w=1, dy=2, z=3, U=4,
+bias=5, document lengths=6).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+X, WGT, DY, Z, U, BIAS, LENS = range(7)
+
+
+@dataclass(frozen=True)
+class Workload:
+    wid: int
+    name: str
+    kind: str            # "dense" (materialised / head-wise) or "lowrank"
+    B: int
+    T: int
+    D: int
+    W: int
+    H: int = 1
+    R: int = 0
+    dtype: str = "bf16"  # "bf16" or "f32"
+    w_std: float = 0.5
+    w_tap0: float = 0.0  # added to tap k = 0
+    packed: bool = False
+    doc_min: int = 128
+    doc_max: int = 4096
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.T
+
+
+WORKLOADS = {
+    1: Workload(1, "tiny_fp32", "dense", 1, 128, 64, 4, H=1, dtype="f32", w_std=0.5),
+    2: Workload(2, "headwise_bf16", "dense", 8, 2048, 2048, 4, H=16, w_std=0.1, w_tap0=0.5),
+    3: Workload(3, "material_bf16", "dense", 4, 4096, 2048, 4, H=1, w_std=math.sqrt(0.1)),
+    4: Workload(4, "lowrank_bf16", "lowrank", 8, 2048, 2048, 4, R=64),
+    5: Workload(5, "qkv_packed_bf16", "dense", 4, 8192, 3072, 4, H=16, w_std=math.sqrt(0.1), packed=True),
+}
+
+
+def by_name(name: str) -> Workload:
+    for w in WORKLOADS.values():
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def custom(B, T, D, W, H=1, R=0, dtype="bf16", seed_id=100, w_std=0.5, w_tap0=0.0, packed=False,
+           doc_min=1, doc_max=None, name="custom") -> Workload:
+    """A workload of arbitrary shape for edge-case tests (seeded by ``seed_id``)."""
+    kind = "lowrank" if R else "dense"
+    return Workload(seed_id, name, kind, B, T, D, W, H=H, R=R, dtype=dtype, w_std=w_std, w_tap0=w_tap0,
+                    packed=packed, doc_min=doc_min, doc_max=doc_max if doc_max is not None else T)
+
+
+def _gen(wid: int, idx: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1000 * wid + idx)
+    return g
+
+
+def _normal(shape, std, wid, idx, dtype):
+    t = torch.randn(*shape, generator=_gen(wid, idx), dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def doc_offsets(wl: Workload) -> torch.Tensor | None:
+    """Packed-document offsets (int32, flattened B*T axis, starts at 0, ends at B*T,
+    contains every sequence start b*T).  None when the workload is not packed."""
+    if not wl.packed:
+        return None
+    g = _gen(wl.wid, LENS)
+    offs = [0]
+    for b in range(wl.B):
+        pos = 0
+        while pos < wl.T:
+            n = int(torch.randint(wl.doc_min, wl.doc_max + 1, (1,), generator=g).item())
+            n = min(n, wl.T - pos)
+            pos += n
+            offs.append(b * wl.T + pos)
+    return torch.tensor(offs, dtype=torch.int32)
+
+
+def make(wl: Workload, with_grad: bool = True) -> dict:
+    """All inputs of one workload as CPU tensors."""
+    dt = wl.torch_dtype
+    out = {"x": _normal((wl.B, wl.T, wl.D), 1.0, wl.wid, X, dt)}
+    if wl.kind == "dense":
+        w = torch.randn(wl.B, wl.T, wl.D // wl.H, wl.W, generator=_gen(wl.wid, WGT), dtype=torch.float32)
+        w.mul_(wl.w_std)
+        if wl.w_tap0:
+            w[..., 0] += wl.w_tap0
+        out["w"] = w.to(dt)
+    else:
+        out["z"] = _normal((wl.B, wl.T, wl.R), 1.0, wl.wid, Z, dt)
+        out["U"] = _normal((wl.R, wl.D * wl.W), 1.0 / math.sqrt(wl.R), wl.wid, U, dt)
+        out["bias"] = _normal((wl.D * wl.W,), 0.1, wl.wid, BIAS, torch.float32)
+    if with_grad:
+        out["dy"] = _normal((wl.B, wl.T, wl.D), 1.0, wl.wid, DY, dt)
+    out["cu_seqlens"] = doc_offsets(wl)
+    return out
+
+
+def shrink(wl: Workload, T: int) -> Workload:
+    """The same workload with a shorter sequence (for oracle-sized parity runs)."""
+    return replace(wl, T=T)
