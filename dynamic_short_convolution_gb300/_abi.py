@@ -1,0 +1,193 @@
+"""ctypes binding of libdsc.so -- argument marshalling only.
+
+Each function here has the name of the C entry point it calls (see
+``include/dsc.h``) and does nothing but check and pass arguments: every step
+of the computation runs in the library's CUDA kernels.  PyTorch supplies device
+memory and the current stream.  There is no fallback: if ``libdsc.so`` is
+missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsc.so")
+
+DSC_OK, DSC_ERR_INVALID_ARG, DSC_ERR_UNSUPPORTED, DSC_ERR_CUDA, DSC_ERR_TIMEOUT = range(5)
+DSC_F32, DSC_BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+# (name, restype, argtypes) of every exported entry point.
+_vp, _i, _u64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong, ctypes.c_size_t
+SIGNATURES = {
+    "dsc_version": (_i, []),
+    "dsc_status_string": (ctypes.c_char_p, [_i]),
+    "dsc_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "dsc_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "dsc_lowrank_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "dsc_lowrank_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "dsc_lowrank_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i,
+                             _vp]),
+    "dsc_validate_cu_seqlens": (_i, [_vp, _i, _i, _i, _vp]),
+    "dsc_sync_status": (_i, [_vp]),
+    "dsc_test_wait_timeout": (_i, [_u64, _vp]),
+}
+
+
+class DscError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libdsc.so is not built ({LIB_PATH}); run "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().dsc_status_string(int(s)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != DSC_OK:
+        raise DscError(what, status)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DSC_BF16
+    if t.dtype == torch.float32:
+        return DSC_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _cu(cu_seqlens):
+    if cu_seqlens is None:
+        return None, 0
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    return cu_seqlens.data_ptr(), cu_seqlens.numel() - 1
+
+
+def dsc_version() -> int:
+    return lib().dsc_version()
+
+
+def dsc_fwd(x, w, y=None, *, cu_seqlens=None, stream=None):
+    """y = x + dynamic conv(x) with w [B,T,D/H,W] (materialised H=1 or head-wise)."""
+    B, T, D = x.shape
+    G, W = w.shape[2], w.shape[3]
+    if tuple(w.shape[:2]) != (B, T) or G < 1 or D % G:
+        raise ValueError("w must be [B, T, D/H, W]")
+    if y is None:
+        y = torch.empty_like(x)
+    cu, n = _cu(cu_seqlens)
+    s = lib().dsc_fwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(y, "y", x.dtype), B, T, D, W, D // G, _dt(x),
+                      cu, n, _stream(stream))
+    _check(s, "dsc_fwd")
+    return y
+
+
+def dsc_bwd(x, w, dy, dx=None, dw=None, *, cu_seqlens=None, stream=None):
+    """(dx, dw) of the forward pass for the upstream gradient dy."""
+    B, T, D = x.shape
+    G, W = w.shape[2], w.shape[3]
+    if tuple(w.shape[:2]) != (B, T) or G < 1 or D % G or tuple(dy.shape) != (B, T, D):
+        raise ValueError("shapes: x, dy [B,T,D]; w [B,T,D/H,W]")
+    dx = torch.empty_like(x) if dx is None else dx
+    dw = torch.empty_like(w) if dw is None else dw
+    cu, n = _cu(cu_seqlens)
+    s = lib().dsc_bwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(dy, "dy", x.dtype), _dev(dx, "dx", x.dtype),
+                      _dev(dw, "dw", x.dtype), B, T, D, W, D // G, _dt(x), cu, n, _stream(stream))
+    _check(s, "dsc_bwd")
+    return dx, dw
+
+
+def dsc_lowrank_fwd(x, z, U, bias, y=None, *, cu_seqlens=None, stream=None):
+    """y = x + dynamic conv(x) with the filter zU + bias formed on chip."""
+    B, T, D = x.shape
+    R = z.shape[-1]
+    if U.shape[0] != R or U.shape[1] % D:
+        raise ValueError("U must be [R, D*W]")
+    W = U.shape[1] // D
+    y = torch.empty_like(x) if y is None else y
+    cu, n = _cu(cu_seqlens)
+    s = lib().dsc_lowrank_fwd(_dev(x, "x"), _dev(z, "z", x.dtype), _dev(U, "U", x.dtype),
+                              _dev(bias, "bias", torch.float32), _dev(y, "y", x.dtype), B, T, D, W, R, _dt(x), cu,
+                              n, _stream(stream))
+    _check(s, "dsc_lowrank_fwd")
+    return y
+
+
+def dsc_lowrank_bwd_workspace_bytes(B, T, D, W, R) -> int:
+    return int(lib().dsc_lowrank_bwd_workspace_bytes(B, T, D, W, R))
+
+
+def dsc_lowrank_bwd(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=None, workspace=None, *, cu_seqlens=None,
+                    stream=None):
+    """(dx, dz, dU, db) of the low-rank forward pass; dU and db are fp32."""
+    B, T, D = x.shape
+    R = z.shape[-1]
+    W = U.shape[1] // D
+    dx = torch.empty_like(x) if dx is None else dx
+    dz = torch.empty_like(z) if dz is None else dz
+    dU = torch.empty(U.shape, dtype=torch.float32, device=x.device) if dU is None else dU
+    db = torch.empty(bias.shape, dtype=torch.float32, device=x.device) if db is None else db
+    nbytes = dsc_lowrank_bwd_workspace_bytes(B, T, D, W, R)
+    if workspace is None and nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    ws = None if not nbytes else _dev(workspace, "workspace")
+    cu, n = _cu(cu_seqlens)
+    s = lib().dsc_lowrank_bwd(_dev(x, "x"), _dev(z, "z", x.dtype), _dev(U, "U", x.dtype),
+                              _dev(bias, "bias", torch.float32), _dev(dy, "dy", x.dtype), _dev(dx, "dx", x.dtype),
+                              _dev(dz, "dz", x.dtype), _dev(dU, "dU", torch.float32),
+                              _dev(db, "db", torch.float32), ws, B, T, D, W, R, _dt(x), cu, n, _stream(stream))
+    _check(s, "dsc_lowrank_bwd")
+    return dx, dz, dU, db
+
+
+def dsc_validate_cu_seqlens(cu_seqlens, B, T, *, stream=None) -> None:
+    cu, n = _cu(cu_seqlens)
+    _check(lib().dsc_validate_cu_seqlens(cu, n, B, T, _stream(stream)), "dsc_validate_cu_seqlens")
+
+
+def dsc_sync_status(*, stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    return int(lib().dsc_sync_status(_stream(stream)))
+
+
+def dsc_test_wait_timeout(limit_ns: int, *, stream=None) -> None:
+    _check(lib().dsc_test_wait_timeout(int(limit_ns), _stream(stream)), "dsc_test_wait_timeout")

@@ -1,0 +1,73 @@
+// dsc_internal.h -- host-side plumbing shared by the libdsc translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "dsc.h"
+
+namespace dsc {
+
+// Arguments of the materialised / head-wise forward and backward passes.
+struct DenseArgs {
+    const void *x = nullptr;
+    const void *w = nullptr;
+    const void *dy = nullptr;
+    void *y = nullptr;
+    void *dx = nullptr;
+    void *dw = nullptr;
+    int B = 0, T = 0, D = 0, W = 0, H = 0;
+    dsc_dtype dt = DSC_BF16;
+    const int32_t *cu = nullptr;
+    int n_docs = 0;
+    cudaStream_t stream = nullptr;
+};
+
+// Arguments of the low-rank forward and backward passes.
+struct LowrankArgs {
+    const void *x = nullptr;
+    const void *z = nullptr;
+    const void *U = nullptr;
+    const float *bias = nullptr;
+    const void *dy = nullptr;
+    void *y = nullptr;
+    void *dx = nullptr;
+    void *dz = nullptr;
+    float *dU = nullptr;
+    float *db = nullptr;
+    void *workspace = nullptr;
+    int B = 0, T = 0, D = 0, W = 0, R = 0;
+    const int32_t *cu = nullptr;
+    int n_docs = 0;
+    cudaStream_t stream = nullptr;
+};
+
+dsc_status dense_fwd(const DenseArgs &a);
+dsc_status dense_bwd(const DenseArgs &a);
+dsc_status lowrank_fwd(const LowrankArgs &a);
+dsc_status lowrank_bwd(const LowrankArgs &a);
+size_t lowrank_bwd_workspace(int B, int T, int D, int W, int R);
+
+// Per-device status word (device address) and the current wait limit.
+int *device_status_word();
+unsigned long long wait_limit_ns();
+
+// Device facts of the current device (cached per device).
+struct DeviceInfo {
+    int device = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+};
+bool device_info(DeviceInfo *out);
+
+// 2-D tiled TMA descriptor: dims {inner, outer}, row pitch in bytes, box
+// {box_inner, box_outer}, zero fill outside the tensor.
+bool encode_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, unsigned long long inner,
+                    unsigned long long outer, unsigned long long row_bytes, unsigned box_inner, unsigned box_outer,
+                    CUtensorMapSwizzle swizzle);
+
+inline dsc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSC_OK : DSC_ERR_CUDA; }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<unsigned long long>(p) & 15ull) == 0; }
+
+}  // namespace dsc

@@ -1,0 +1,171 @@
+/*
+ * dsc.h -- C ABI of libdsc.so, the GB300 (sm_103a) dynamic short convolution.
+ *
+ * The operation (notes on "Dynamic Short Convolutions Improve Transformers",
+ * section "Parameterization", eq. 2, applied as a residual as in eq. 3 of
+ * section "Placement"):
+ *
+ *     y[t,d] = x[t,d] + sum_{k=0}^{W-1} w[t, g(d), k] * x~[t-k, d]
+ *
+ * a causal depthwise convolution along time whose filter is generated per
+ * token.  g(d) = floor(d / H): H is the head SIZE -- H consecutive channels
+ * share one filter ("head-wise parameterization"); H = 1 is the materialised
+ * per-channel filter.  x~[j, d] = x[j, d] when token j lies in token t's
+ * document, else 0: zero history before every sequence start and, with
+ * packed documents, before every document start (the boundary rule of the
+ * notes on "RubiConv - Efficient Boundary-Respecting Convolutions", section
+ * "Key design 1").  The residual term x[t,d] is never masked.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layout.  Row-major, contiguous, tokens on a flattened B*T axis:
+ *     x, y, dy, dx     [B, T, D]
+ *     w, dw            [B, T, D/H, W]     (tap index k innermost; k = 0 is the
+ *                                          current token, k = j reaches back j)
+ *     z, dz            [B, T, R]
+ *     U, dU            [R, D*W]           (filter column n = d*W + k)
+ *     bias, db         [D*W]              (fp32)
+ *     cu_seqlens       [n_docs + 1] int32 offsets on the flattened axis
+ *                      (0 = cu[0] < cu[1] < ... < cu[n_docs] = B*T).  Every
+ *                      sequence start b*T is a document start whether or not it
+ *                      is listed.  NULL: each sequence is one document.
+ *  Ownership.  Every pointer is caller-owned DEVICE memory of the current
+ *     device, 16-byte aligned for the vectorised paths (any element-aligned
+ *     pointer is accepted and routed to a scalar path).  The library
+ *     allocates no device memory and keeps no per-call state; it caches the
+ *     SM count and kernel attributes per device.
+ *  Semantics.  Outputs are OVERWRITTEN (never accumulated).  Calls are
+ *     asynchronous on `stream` and return after the launches are queued.
+ *     Inputs and outputs must not overlap.
+ *  Precision.  bf16 (or fp32) storage, fp32 arithmetic, results rounded to
+ *     nearest-even on store.
+ *  Errors.  Arguments are validated before any launch; a rejected call
+ *     launches nothing and returns DSC_ERR_INVALID_ARG or
+ *     DSC_ERR_UNSUPPORTED.  A failed launch returns DSC_ERR_CUDA.  Kernels
+ *     never trap: a device-side wait that exceeds its time limit records
+ *     DSC_ERR_TIMEOUT in a device status word, which dsc_sync_status()
+ *     reports.  Nothing aborts, exits or throws across this ABI.
+ *  Malformed cu_seqlens (not increasing, wrong ends) cannot make a kernel
+ *     read or write out of bounds; the results are then unspecified.
+ *     dsc_validate_cu_seqlens() checks them on the device.
+ */
+#ifndef DSC_H
+#define DSC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSC_OK = 0,
+    DSC_ERR_INVALID_ARG = 1, /* bad size, null pointer, D % H != 0, ... */
+    DSC_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. fp32 low-rank) */
+    DSC_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    DSC_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up */
+} dsc_status;
+
+typedef enum { DSC_F32 = 0, DSC_BF16 = 1 } dsc_dtype;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int dsc_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *dsc_status_string(dsc_status s);
+
+/*
+ * dsc_fwd -- forward pass, materialised (H = 1) or head-wise (H > 1) filter.
+ *   "Parameterization", eq. 2, with the residual of eq. 3.
+ *   x [B,T,D], w [B,T,D/H,W] in dtype dt; writes y [B,T,D].
+ *   Requirements: B, T, D >= 1; 1 <= W <= 8; H >= 1 and D % H == 0;
+ *   B*T*D < 2^31; cu_seqlens NULL or n_docs >= 1.
+ *   Reads every input once and writes y once ("Efficient training": the
+ *   kernel reads activations and weights once and keeps the convolution on
+ *   chip).
+ */
+dsc_status dsc_fwd(const void *x, const void *w, void *y, int B, int T, int D, int W, int H, dsc_dtype dt,
+                   const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
+
+/*
+ * dsc_bwd -- backward pass of dsc_fwd for an upstream gradient dy.
+ *   The derivative of eq. 2 + eq. 3:
+ *     dx[s,d]   = dy[s,d] + sum_{k<W, s+k in s's document} w[s+k, g(d), k] dy[s+k, d]
+ *     dw[t,g,k] = sum_{d : g(d) = g} dy[t,d] * x~[t-k, d]
+ *   x, w, dy in dtype dt; writes dx [B,T,D] and dw [B,T,D/H,W] (both fully
+ *   overwritten).  Same requirements as dsc_fwd.
+ */
+dsc_status dsc_bwd(const void *x, const void *w, const void *dy, void *dx, void *dw, int B, int T, int D, int W,
+                   int H, dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
+
+/*
+ * dsc_lowrank_fwd -- forward pass with the low-rank filter generator fused.
+ *   "Parameterization" (low-rank D -> R -> W*D, every transform with a bias)
+ *   and "Efficient training" (the second projection fused into the kernel):
+ *     w[t, d, k] = sum_r z[t,r] U[r, d*W+k] + bias[d*W+k]
+ *   is formed on chip (tensor cores, fp32 accumulation) and never written to
+ *   memory, then eq. 2 + eq. 3 with H = 1.
+ *   x [B,T,D], z [B,T,R], U [R,D*W] in bf16, bias [D*W] fp32; writes y.
+ *   Requirements: dt == DSC_BF16 (DSC_F32 -> DSC_ERR_UNSUPPORTED);
+ *   D % 8 == 0; R % 8 == 0 and 8 <= R <= 128; 1 <= W <= 8; pointers 16-byte
+ *   aligned.
+ */
+dsc_status dsc_lowrank_fwd(const void *x, const void *z, const void *U, const float *bias, void *y, int B, int T,
+                           int D, int W, int R, dsc_dtype dt, const int32_t *cu_seqlens, int n_docs,
+                           cudaStream_t stream);
+
+/*
+ * Bytes of caller-provided device workspace dsc_lowrank_bwd needs for these
+ * sizes (0 is a valid answer).  The workspace holds fp32 partial sums.
+ */
+size_t dsc_lowrank_bwd_workspace_bytes(int B, int T, int D, int W, int R);
+
+/*
+ * dsc_lowrank_bwd -- backward pass of dsc_lowrank_fwd.
+ *   With G[t, d*W+k] = dy[t,d] * x~[t-k, d] (the gradient of the generated
+ *   filter, formed on chip) and the filter recomputed on chip:
+ *     dx  as in dsc_bwd with w = zU + bias
+ *     dz[t,r] = sum_n G[t,n] U[r,n]        (bf16 [B,T,R])
+ *     dU[r,n] = sum_t z[t,r] G[t,n]        (fp32 [R, D*W])
+ *     db[n]   = sum_t G[t,n]               (fp32 [D*W])
+ *   `workspace` must hold dsc_lowrank_bwd_workspace_bytes() bytes of device
+ *   memory, 256-byte aligned (may be NULL when that size is 0); its contents on
+ *   entry are ignored.  Same requirements as dsc_lowrank_fwd.
+ */
+dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const float *bias, const void *dy, void *dx,
+                           void *dz, float *dU, float *db, void *workspace, int B, int T, int D, int W, int R,
+                           dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
+
+/*
+ * dsc_validate_cu_seqlens -- device-side check of packed-document offsets:
+ * cu[0] == 0, strictly increasing, cu[n_docs] == B*T.  Asynchronous; a
+ * violation is recorded as DSC_ERR_INVALID_ARG in the device status word,
+ * read by dsc_sync_status().
+ */
+dsc_status dsc_validate_cu_seqlens(const int32_t *cu_seqlens, int n_docs, int B, int T, cudaStream_t stream);
+
+/*
+ * dsc_sync_status -- synchronise `stream`, then read and clear the device
+ * status word of the current device.  Returns DSC_OK, DSC_ERR_TIMEOUT (a
+ * kernel's bounded wait gave up), DSC_ERR_INVALID_ARG (a failed
+ * dsc_validate_cu_seqlens) or DSC_ERR_CUDA.
+ */
+dsc_status dsc_sync_status(cudaStream_t stream);
+
+/*
+ * dsc_test_wait_timeout -- test hook for the failure path.  Launches one tiny
+ * kernel that waits on a shared-memory barrier nothing ever arrives at, with
+ * the same bounded wait the product kernels use and the given limit in
+ * nanoseconds; when the limit runs out it records DSC_ERR_TIMEOUT in the
+ * device status word (read it with dsc_sync_status) and returns.  Nothing
+ * hangs, traps or faults.  The paper has no counterpart; this exists so the
+ * timeout path can be tested on a GPU.
+ */
+dsc_status dsc_test_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSC_H */

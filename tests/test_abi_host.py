@@ -1,0 +1,76 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point the header declares, and rejects bad arguments before
+launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsc.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from dynamic_short_convolution_gb300 import build, _abi
+
+    build.build()
+    return _abi.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsc_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    for n in ("dsc_fwd", "dsc_bwd", "dsc_lowrank_fwd", "dsc_lowrank_bwd", "dsc_lowrank_bwd_workspace_bytes",
+              "dsc_status_string", "dsc_sync_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    from dynamic_short_convolution_gb300 import _abi
+
+    for n in _declared():
+        assert hasattr(L, n), f"libdsc.so does not export {n}"
+        assert n in _abi.SIGNATURES, f"binding has no signature for {n}"
+
+
+def test_status_strings(L):
+    assert L.dsc_status_string(0) == b"DSC_OK"
+    assert L.dsc_status_string(4) == b"DSC_ERR_TIMEOUT"
+    assert L.dsc_version() >= 10000
+
+
+def test_rejects_bad_arguments_before_any_launch(L):
+    p = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    bf16, f32 = 1, 0
+    # non-positive sizes, W out of range, D % H != 0, bad dtype, n_docs < 1 with offsets
+    assert L.dsc_fwd(p, p, p, 0, 8, 64, 4, 1, bf16, None, 0, None) == 1
+    assert L.dsc_fwd(p, p, p, 1, 8, 64, 9, 1, bf16, None, 0, None) == 1
+    assert L.dsc_fwd(p, p, p, 1, 8, 64, 0, 1, bf16, None, 0, None) == 1
+    assert L.dsc_fwd(p, p, p, 1, 8, 64, 4, 3, bf16, None, 0, None) == 1
+    assert L.dsc_fwd(p, p, p, 1, 8, 64, 4, 1, 7, None, 0, None) == 1
+    assert L.dsc_fwd(p, p, p, 1, 8, 64, 4, 1, bf16, p, 0, None) == 1
+    assert L.dsc_fwd(None, p, p, 1, 8, 64, 4, 1, bf16, None, 0, None) == 1
+    assert L.dsc_fwd(ctypes.c_void_p(0x10001), p, p, 1, 8, 64, 4, 1, bf16, None, 0, None) == 1  # not element-aligned
+    assert L.dsc_bwd(p, p, p, p, None, 1, 8, 64, 4, 1, bf16, None, 0, None) == 1
+    assert L.dsc_fwd(p, p, p, 1 << 16, 1 << 16, 8, 4, 1, bf16, None, 0, None) == 1  # int32 size limit
+    # low-rank: fp32 unsupported, R out of range unsupported
+    assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 16, f32, None, 0, None) == 2
+    assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 256, bf16, None, 0, None) == 2
+    assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 0, bf16, None, 0, None) == 1
+    assert L.dsc_validate_cu_seqlens(None, 3, 1, 8, None) == 1
+
+
+def test_loading_without_gpu_reports_cuda_error_not_crash(L):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = ctypes.c_void_p(0x10000)
+    assert L.dsc_fwd(p, p, p, 1, 8, 64, 4, 1, 1, None, 0, None) == 3
