@@ -23,6 +23,7 @@ from ._abi import (  # noqa: F401
     DscError,
     dsc_bwd,
     dsc_fwd,
+    dsc_launch_count,
     dsc_lowrank_bwd,
     dsc_lowrank_bwd_workspace_bytes,
     dsc_lowrank_fwd,

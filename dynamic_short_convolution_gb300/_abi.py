@@ -37,6 +37,7 @@ SIGNATURES = {
     "dsc_validate_cu_seqlens": (_i, [_vp, _i, _i, _i, _vp]),
     "dsc_sync_status": (_i, [_vp]),
     "dsc_test_wait_timeout": (_i, [_u64, _vp]),
+    "dsc_launch_count": (_u64, []),
 }
 
 
@@ -187,6 +188,11 @@ def dsc_validate_cu_seqlens(cu_seqlens, B, T, *, stream=None) -> None:
 def dsc_sync_status(*, stream=None) -> int:
     """Synchronise the stream; return (and clear) the device status word."""
     return int(lib().dsc_sync_status(_stream(stream)))
+
+
+def dsc_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().dsc_launch_count())
 
 
 def dsc_test_wait_timeout(limit_ns: int, *, stream=None) -> None:

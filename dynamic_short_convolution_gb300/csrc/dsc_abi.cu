@@ -21,6 +21,9 @@ static int *g_status_ptr[kMaxDevices] = {};
 static DeviceInfo g_dev[kMaxDevices] = {};
 static bool g_dev_ok[kMaxDevices] = {};
 static std::atomic<unsigned long long> g_wait_ns{1000000000ull};  // about one second
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launch(unsigned n) { g_launches.fetch_add(n); }
 
 int *device_status_word()
 {
@@ -243,7 +246,7 @@ dsc_status dsc_validate_cu_seqlens(const int32_t *cu_seqlens, int n_docs, int B,
     int *st = device_status_word();
     if (!st) return DSC_ERR_CUDA;
     validate_cu_kernel<<<1, 256, 0, stream>>>(cu_seqlens, n_docs, static_cast<long long>(B) * T, st);
-    return cuda_status(cudaGetLastError());
+    return launched();
 }
 
 dsc_status dsc_sync_status(cudaStream_t stream)
@@ -263,7 +266,9 @@ dsc_status dsc_test_wait_timeout(unsigned long long limit_ns, cudaStream_t strea
     int *st = device_status_word();
     if (!st) return DSC_ERR_CUDA;
     wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, st);
-    return cuda_status(cudaGetLastError());
+    return launched();
 }
+
+unsigned long long dsc_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"

@@ -263,7 +263,7 @@ static dsc_status launch_bwd_tma(const DenseArgs &a, const DeviceInfo &dev)
     if (e != cudaSuccess) return DSC_ERR_CUDA;
     const DenseParams q = dense_params(a, plan, a.dx, a.dw);
     kern<<<plan.grid, plan.threads, plan.smem_bytes, a.stream>>>(tm_x, tm_dy, tm_w, q);
-    return cuda_status(cudaGetLastError());
+    return launched();
 }
 
 template <typename E, int W>
@@ -305,12 +305,12 @@ static dsc_status bwd_scalar(const DenseArgs &a, const DeviceInfo &dev)
     dense_bwd_dx_scalar<E><<<static_cast<int>(b1), 256, 0, a.stream>>>(
         static_cast<const E *>(a.w), static_cast<const E *>(a.dy), static_cast<E *>(a.dx), static_cast<int>(BT), a.T,
         a.D, a.W, a.H, a.cu, a.n_docs);
-    dsc_status s = cuda_status(cudaGetLastError());
+    dsc_status s = launched();
     if (s != DSC_OK) return s;
     dense_bwd_dw_scalar<E><<<static_cast<int>(b2), 256, 0, a.stream>>>(
         static_cast<const E *>(a.x), static_cast<const E *>(a.dy), static_cast<E *>(a.dw), static_cast<int>(BT), a.T,
         a.D, a.W, a.H, a.cu, a.n_docs);
-    return cuda_status(cudaGetLastError());
+    return launched();
 }
 
 dsc_status dense_bwd(const DenseArgs &a)

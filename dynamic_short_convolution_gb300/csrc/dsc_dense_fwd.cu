@@ -200,7 +200,7 @@ static dsc_status launch_fwd_tma(const DenseArgs &a, const DeviceInfo &dev)
     if (e != cudaSuccess) return DSC_ERR_CUDA;
     const DenseParams q = dense_params(a, plan, a.y, nullptr);
     kern<<<plan.grid, plan.threads, plan.smem_bytes, a.stream>>>(tm_x, tm_w, q);
-    return cuda_status(cudaGetLastError());
+    return launched();
 }
 
 template <typename E, int W>
@@ -240,7 +240,7 @@ static dsc_status fwd_scalar(const DenseArgs &a, const DeviceInfo &dev)
     dense_fwd_scalar<E><<<static_cast<int>(blocks), 256, 0, a.stream>>>(
         static_cast<const E *>(a.x), static_cast<const E *>(a.w), static_cast<E *>(a.y), a.B * a.T, a.T, a.D, a.W,
         a.H, a.cu, a.n_docs);
-    return cuda_status(cudaGetLastError());
+    return launched();
 }
 
 // Path selection: the TMA kernel whenever its alignment rules hold, else the scalar kernel.

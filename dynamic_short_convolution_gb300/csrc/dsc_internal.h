@@ -66,7 +66,18 @@ bool encode_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype,
                     unsigned long long outer, unsigned long long row_bytes, unsigned box_inner, unsigned box_outer,
                     CUtensorMapSwizzle swizzle);
 
+// Count one kernel launch (process-wide; reported by dsc_launch_count).
+void count_launch(unsigned n = 1);
+
 inline dsc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSC_OK : DSC_ERR_CUDA; }
+
+// Status of a launch that was just queued: counts it when it succeeded.
+inline dsc_status launched(unsigned n = 1)
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launch(n);
+    return cuda_status(e);
+}
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<unsigned long long>(p) & 15ull) == 0; }
 

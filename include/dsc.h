@@ -155,6 +155,13 @@ dsc_status dsc_validate_cu_seqlens(const int32_t *cu_seqlens, int n_docs, int B,
 dsc_status dsc_sync_status(cudaStream_t stream);
 
 /*
+ * dsc_launch_count -- number of kernels this library has launched in this
+ * process, on any device (a monotonically increasing counter; for
+ * accounting in benchmarks).
+ */
+unsigned long long dsc_launch_count(void);
+
+/*
  * dsc_test_wait_timeout -- test hook for the failure path.  Launches one tiny
  * kernel that waits on a shared-memory barrier nothing ever arrives at, with
  * the same bounded wait the product kernels use and the given limit in
