@@ -5,8 +5,10 @@ Metric: fwd+bwd tokens/s and achieved HBM GB/s (fraction of the measured HBM
 roofline).  One step = one forward (dsc_fwd) and one backward (dsc_bwd) pass
 over one batch of the head-wise bf16 workload (B=8, T=2048, D=2048, W=4,
 H=16: Q/K/V-sized activations at about 2B-model width, the shape on which the
-pages quote their head-wise kernel) with inputs resident in HBM.  L2 is
-flushed (512 MiB write) between timed steps, outside the timed events.
+pages quote their head-wise kernel) with inputs resident in HBM.  Steps run
+back to back and rotate over independent copies of the workload's tensors
+(at least 600 MB together, several times the 129 MB L2), so every step reads
+inputs that are not in L2 and each kernel pays for its own write-backs.
 
 Prints ONE JSON line on rank 0.  Multi-GPU (torchrun) runs one independent
 replica per GPU ("weak" scaling; the path shards by batch with no exchange).
@@ -34,7 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "dyn-conv fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 roofline)"
 UNIT = "tokens/s"
 MAIN_WORKLOAD = "headwise_bf16"
-FLUSH_BYTES = 512 << 20
+ROTATE_BYTES = 600 << 20  # minimum bytes across the rotating copies
 
 
 def parse():
@@ -153,6 +155,24 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- workloads on the GPU
 
+class _Sets:
+    """Independent copies of one workload's device tensors; step i uses copy i % n."""
+
+    def __init__(self, tensors: dict, per_copy_bytes: int, min_copies: int = 2):
+        import torch
+
+        n = max(min_copies, -(-ROTATE_BYTES // max(per_copy_bytes, 1)))
+        self.n = n
+        self.sets = [tensors] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
+                                 for _ in range(n - 1)]
+        self.i = 0
+
+    def next(self):
+        s = self.sets[self.i % self.n]
+        self.i += 1
+        return s
+
+
 class DenseProblem:
     def __init__(self, wl, dev):
         import torch
@@ -163,114 +183,137 @@ class DenseProblem:
         d = inputs.make(wl)
         self.host = d
         g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
-        self.x, self.w, self.dy, self.cu = g["x"], g["w"], g["dy"], g["cu_seqlens"]
-        self.y = torch.empty_like(self.x)
-        self.dx = torch.empty_like(self.x)
-        self.dw = torch.empty_like(self.w)
-        es = self.x.element_size()
-        xb, wb = self.x.numel() * es, self.w.numel() * es
-        cb = 0 if self.cu is None else self.cu.numel() * 4
+        t = {"x": g["x"], "w": g["w"], "dy": g["dy"], "cu": g["cu_seqlens"], "y": torch.empty_like(g["x"]),
+             "dx": torch.empty_like(g["x"]), "dw": torch.empty_like(g["w"])}
+        es = g["x"].element_size()
+        xb, wb = g["x"].numel() * es, g["w"].numel() * es
+        cb = 0 if g["cu_seqlens"] is None else g["cu_seqlens"].numel() * 4
         self.bytes_fwd = 2 * xb + wb + cb
         self.bytes_bwd = 3 * xb + 2 * wb + cb
         self.flops_fwd = self.flops_bwd = 0
+        self.rot = _Sets(t, 4 * xb + 2 * wb)
+        self.cur = t
+
+    def __getattr__(self, name):  # the current copy's tensors (x, w, dy, y, dx, dw)
+        cur = self.__dict__.get("cur")
+        if cur is not None and name in cur:
+            return cur[name]
+        raise AttributeError(name)
+
+    def advance(self):
+        self.cur = self.rot.next()
 
     def fwd(self):
         import dynamic_short_convolution_gb300 as dsc
 
-        dsc.dsc_fwd(self.x, self.w, self.y, cu_seqlens=self.cu)
+        c = self.cur
+        dsc.dsc_fwd(c["x"], c["w"], c["y"], cu_seqlens=c["cu"])
 
     def bwd(self):
         import dynamic_short_convolution_gb300 as dsc
 
-        dsc.dsc_bwd(self.x, self.w, self.dy, self.dx, self.dw, cu_seqlens=self.cu)
+        c = self.cur
+        dsc.dsc_bwd(c["x"], c["w"], c["dy"], c["dx"], c["dw"], cu_seqlens=c["cu"])
 
 
 class LowrankProblem:
     def __init__(self, wl, dev):
         import torch
 
+        import dynamic_short_convolution_gb300 as dsc
         from dynamic_short_convolution_gb300 import inputs
 
         self.wl = wl
         d = inputs.make(wl)
         self.host = d
         g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
-        self.x, self.z, self.U, self.b, self.dy, self.cu = g["x"], g["z"], g["U"], g["bias"], g["dy"], g["cu_seqlens"]
-        self.y = torch.empty_like(self.x)
-        self.dx = torch.empty_like(self.x)
-        self.dz = torch.empty_like(self.z)
-        self.dU = torch.empty(self.U.shape, dtype=torch.float32, device=dev)
-        self.db = torch.empty(self.b.shape, dtype=torch.float32, device=dev)
-        import dynamic_short_convolution_gb300 as dsc
-
         nb = dsc.dsc_lowrank_bwd_workspace_bytes(wl.B, wl.T, wl.D, wl.W, wl.R)
-        self.ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+        t = {"x": g["x"], "z": g["z"], "U": g["U"], "bias": g["bias"], "dy": g["dy"], "cu": g["cu_seqlens"],
+             "y": torch.empty_like(g["x"]), "dx": torch.empty_like(g["x"]), "dz": torch.empty_like(g["z"]),
+             "dU": torch.empty(g["U"].shape, dtype=torch.float32, device=dev),
+             "db": torch.empty(g["bias"].shape, dtype=torch.float32, device=dev),
+             "ws": torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)}
         es = 2
-        xb, zb, ub = self.x.numel() * es, self.z.numel() * es, self.U.numel() * es
+        xb, zb, ub = g["x"].numel() * es, g["z"].numel() * es, g["U"].numel() * es
         nw = wl.D * wl.W
         self.bytes_fwd = 2 * xb + zb + ub + 4 * nw
         self.bytes_bwd = 3 * xb + 2 * zb + ub + 4 * nw + 4 * wl.R * nw + 4 * nw
         m = wl.B * wl.T
         self.flops_fwd = 2 * m * nw * wl.R
         self.flops_bwd = 3 * 2 * m * nw * wl.R  # filter recompute + dz + dU
+        self.rot = _Sets(t, 4 * xb + 3 * zb)
+        self.cur = t
+
+    def __getattr__(self, name):
+        cur = self.__dict__.get("cur")
+        if cur is not None and name in cur:
+            return cur[name]
+        raise AttributeError(name)
+
+    def advance(self):
+        self.cur = self.rot.next()
 
     def fwd(self):
         import dynamic_short_convolution_gb300 as dsc
 
-        dsc.dsc_lowrank_fwd(self.x, self.z, self.U, self.b, self.y, cu_seqlens=self.cu)
+        c = self.cur
+        dsc.dsc_lowrank_fwd(c["x"], c["z"], c["U"], c["bias"], c["y"], cu_seqlens=c["cu"])
 
     def bwd(self):
         import dynamic_short_convolution_gb300 as dsc
 
-        dsc.dsc_lowrank_bwd(self.x, self.z, self.U, self.b, self.dy, self.dx, self.dz, self.dU, self.db, self.ws,
-                            cu_seqlens=self.cu)
+        c = self.cur
+        dsc.dsc_lowrank_bwd(c["x"], c["z"], c["U"], c["bias"], c["dy"], c["dx"], c["dz"], c["dU"], c["db"],
+                            c["ws"], cu_seqlens=c["cu"])
 
 
 def make_problem(wl, dev):
     return LowrankProblem(wl, dev) if wl.kind == "lowrank" else DenseProblem(wl, dev)
 
 
-def time_steps(prob, flush, steps):
-    """Per-step device times (ms) of fwd, bwd and both, each step after an L2 flush."""
+def time_steps(prob, steps):
+    """Per-step device times (ms) of fwd and bwd; steps back to back on rotating input copies."""
     import torch
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for e0, e1, e2 in ev:
-        flush.zero_()
-        e0.record()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
+    ev[0].record()
+    for i in range(steps):
+        prob.advance()
         prob.fwd()
-        e1.record()
+        ev[2 * i + 1].record()
         prob.bwd()
-        e2.record()
+        ev[2 * i + 2].record()
     torch.cuda.synchronize()
-    f = [a.elapsed_time(b) for a, b, _ in ev]
-    b = [b_.elapsed_time(c) for _, b_, c in ev]
+    f = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+    b = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(steps)]
     return f, b
 
 
 # ----------------------------------------------------------------- CPU oracle arm
 
 def oracle_tokens_per_s(wl, budget_s, min_tokens=64):
-    """fp64 oracle fwd+bwd on a token range of the workload, grown until it takes about budget_s."""
+    """fp64 oracle fwd+bwd over consecutive token ranges of the workload (wrapping around), until about
+    budget_s of CPU time has been spent; returns (tokens/s, tokens, seconds)."""
     import oracle
     from dynamic_short_convolution_gb300 import inputs
 
     d = inputs.make(wl)
     oracle.build()
     BT = wl.B * wl.T
-    n = min_tokens
-    spent, done = 0.0, 0
-    # calibrate on a short range, then run one range sized for the budget
     t0 = time.perf_counter()
-    _oracle_step(oracle, wl, d, 0, n)
-    dt = time.perf_counter() - t0
-    per_tok = dt / n
-    n2 = int(max(min_tokens, min(BT, (budget_s - dt) / max(per_tok, 1e-9))))
+    _oracle_step(oracle, wl, d, 0, min_tokens)
+    per_tok = (time.perf_counter() - t0) / min_tokens
+    chunk = int(max(min_tokens, min(BT, 0.25 * budget_s / max(per_tok, 1e-9))))
+    done, pos = 0, 0
     t1 = time.perf_counter()
-    _oracle_step(oracle, wl, d, 0, n2)
-    spent = time.perf_counter() - t1
-    done = n2
+    while True:
+        n = min(chunk, BT - pos)
+        _oracle_step(oracle, wl, d, pos, pos + n)
+        done += n
+        pos = (pos + n) % BT
+        spent = time.perf_counter() - t1
+        if spent >= budget_s:
+            break
     return done / spent, done, spent
 
 
@@ -335,7 +378,7 @@ def workload_config(wl, world):
     shape = f"B={wl.B} T={wl.T} D={wl.D} W={wl.W}" + (f" R={wl.R}" if wl.kind == "lowrank" else f" H={wl.H}")
     return {"workload": f"{wl.name}: {shape}" + (" packed documents" if wl.packed else ""),
             "global_batch": wl.B * world, "seq_len": wl.T, "parallelism": "replicas (one independent batch per GPU)",
-            "l2": "flushed between timed steps (512 MiB write, outside the timed events)"}
+            "l2": "inputs larger than L2: steps back to back over rotating copies of the tensors (>= 600 MB)"}
 
 
 # ----------------------------------------------------------------- main arm
@@ -356,7 +399,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         v, n, spent = oracle_tokens_per_s(wl, budget_s=12.0)
         cpu = {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-               "sample": f"{n} consecutive tokens (all {wl.D} channels) of {wl.name}, fwd + bwd, {spent:.1f} s"}
+               "sample": f"{n} tokens (all {wl.D} channels; consecutive ranges of {wl.name}, wrapping) fwd + bwd "
+                         f"in {spent:.1f} s"}
 
     import torch
     import torch.distributed as dist
@@ -375,11 +419,10 @@ def main():
             dist.barrier()
 
     hbm_peak, tc_peak, tc_sust, peak_src = peaks()
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     prob = make_problem(wl, dev)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        prob.advance()
         prob.fwd()
         prob.bwd()
     torch.cuda.synchronize()
@@ -393,7 +436,7 @@ def main():
     torch.cuda.synchronize()
     launches0 = dsc.dsc_launch_count()
     t_wall0 = time.perf_counter()
-    f_ms, b_ms = time_steps(prob, flush, args.steps)
+    f_ms, b_ms = time_steps(prob, args.steps)
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.perf_counter()
@@ -429,11 +472,11 @@ def main():
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(prob, flush, max(10, min(args.steps // 10, 200)), dev, world)
+        e2e = measure_e2e(prob, max(10, min(args.steps // 10, 200)), dev, world)
 
     rows = None
     if rank == 0 and world == 1 and not args.no_rows:
-        rows = measure_rows(dev, flush, hbm_peak, tc_peak)
+        rows = measure_rows(dev, hbm_peak, tc_peak)
 
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     if rank == 0:
@@ -453,7 +496,7 @@ def main():
     return 0
 
 
-def measure_e2e(prob, flush, steps, dev, world):
+def measure_e2e(prob, steps, dev, world):
     """The same metric through the public API with pinned host buffers: every step copies the inputs
     host->device, runs fwd+bwd, and copies the results device->host, all inside the timed events."""
     import torch
@@ -466,20 +509,15 @@ def measure_e2e(prob, flush, steps, dev, world):
     h_in = {n: prob.host[n].pin_memory() for n in names_in}
     h_out = {n: torch.empty(getattr(prob, n).shape, dtype=getattr(prob, n).dtype, pin_memory=True)
              for n in names_out}
-    dev_in = {"x": prob.x, "dy": prob.dy}
-    if wl.kind == "lowrank":
-        dev_in.update({"z": prob.z, "U": prob.U, "bias": prob.b})
-    else:
-        dev_in["w"] = prob.w
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
     times = []
     for i in range(steps + 3):
-        flush.zero_()
+        prob.advance()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for n in names_in:
-            dev_in[n].copy_(h_in[n], non_blocking=True)
+            getattr(prob, n).copy_(h_in[n], non_blocking=True)
         prob.fwd()
         prob.bwd()
         for n in names_out:
@@ -499,7 +537,7 @@ def measure_e2e(prob, flush, steps, dev, world):
             "api": "dynamic_short_convolution_gb300.dsc_fwd / dsc_bwd (or dsc_lowrank_*) on pinned host copies"}
 
 
-def measure_rows(dev, flush, hbm_peak, tc_peak):
+def measure_rows(dev, hbm_peak, tc_peak):
     """Every workload, timed the same way (fewer steps): fwd / bwd device time and roofline fractions."""
     import torch
 
@@ -511,11 +549,11 @@ def measure_rows(dev, flush, hbm_peak, tc_peak):
         try:
             prob = make_problem(wl, dev)
             for _ in range(3):
-                flush.zero_()
+                prob.advance()
                 prob.fwd()
                 prob.bwd()
             torch.cuda.synchronize()
-            f, b = time_steps(prob, flush, 50)
+            f, b = time_steps(prob, 100)
         except dsc.DscError as e:
             out[wl.name] = {"status": str(e)}
             continue

@@ -123,50 +123,79 @@ __global__ void __launch_bounds__(32 * (1 + TileCfg<E, HPT, true>::NCW), 1)
             E *dw = reinterpret_cast<E *>(p.out1);
             const int head = c >> p.hshift;  // global head of this lane's first channel
 
-            float xw[W][8];   // xw[k] = x at token (t - k)
-            float acc[W][8];  // acc[k] = partial dx of token (t - k)
+            // Rings indexed by step r (token t0+r0+r): the x window (slot ring(r, W) holds the x row of
+            // step r) and the dx accumulators (slot ring(r, W) collects the gradient of step r's token).
+            float2 xw[W][4];
+            float2 acc[W][4];
 #pragma unroll
-            for (int k = 1; k < W; ++k) load8(xs + (r0 + W - 1 - k) * kDC, xw[k]);
+            for (int r = -(W - 1); r < 0; ++r) load8x2(xs + (r0 + r + W - 1) * kDC, xw[ring(r, W)]);
 #pragma unroll
             for (int k = 0; k < W; ++k)
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[k][q] = 0.f;
+                for (int i = 0; i < 4; ++i) acc[k][i] = make_float2(0.f, 0.f);
 
 #pragma unroll
             for (int r = 0; r < RPW + W - 1; ++r) {
                 const int j = r0 + r;  // tile-local token of this step
-                float g[8];
-                load8(gs + j * kDC, g);
+                float2 g[4];
+                load8x2(gs + j * kDC, g);
                 float wv[NWV];
                 load_n<E, NWV>(ws + j * p.w_box, wv);
+                float2 wp[4][W];
+                filter_pairs<HPT, W>(wv, wp);
                 const int nv = nvs[j];
-                // ring: slot 0 starts the gradient of token j with the residual term
+                // dx: the residual opens this token's slot; w[j,k] * dy[j] goes to token j-k
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[0][q] = g[q];
+                for (int i = 0; i < 4; ++i) acc[ring(r, W)][i] = g[i];
+                if (nv == W) {
 #pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    if (k < nv) {
+                    for (int k = 0; k < W; ++k)
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) acc[k][q] = fmaf(wv[((q * HPT) / 8) * W + k], g[q], acc[k][q]);
-                    }
+                        for (int i = 0; i < 4; ++i) acc[ring(r - k, W)][i] = fma2(wp[i][k], g[i], acc[ring(r - k, W)][i]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < W; ++k)
+                        if (k < nv) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                acc[ring(r - k, W)][i] = fma2(wp[i][k], g[i], acc[ring(r - k, W)][i]);
+                        }
                 }
-                if (r >= W - 1) {  // token j-(W-1) has received all of its terms
+                if (r >= W - 1) {  // the token of step r-(W-1) has received all of its terms
                     const int tdx = t0 + j - (W - 1);
-                    if (cvalid && tdx < p.BT) store8(dx + static_cast<size_t>(tdx) * p.D + c, acc[W - 1]);
+                    if (cvalid && tdx < p.BT) store8x2(dx + static_cast<size_t>(tdx) * p.D + c, acc[ring(r - (W - 1), W)]);
                 }
-                if (r < RPW) {  // dw of token j
-                    load8(xs + (j + W - 1) * kDC, xw[0]);
+                if (r < RPW) {  // dw of token j: sum over each head's channels of dy * x~
+                    load8x2(xs + (j + W - 1) * kDC, xw[ring(r, W)]);
                     float part[HPT][W];
 #pragma unroll
-                    for (int h = 0; h < HPT; ++h)
+                    for (int k = 0; k < W; ++k) {
+                        const float2(&xk)[4] = xw[ring(r - k, W)];
+                        if constexpr (HPT == 8) {  // one channel per head: plain products
 #pragma unroll
-                        for (int k = 0; k < W; ++k) {
-                            float sacc = 0.f;
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 pr = mul2(g[i], xk[i]);
+                                part[2 * i][k] = pr.x;
+                                part[2 * i + 1][k] = pr.y;
+                            }
+                        } else {
+                            constexpr int PPH = 4 / HPT;  // channel pairs per head
 #pragma unroll
-                            for (int q = h * (8 / HPT); q < (h + 1) * (8 / HPT); ++q) sacc = fmaf(g[q], xw[k][q], sacc);
-                            part[h][k] = k < nv ? sacc : 0.f;
+                            for (int h = 0; h < HPT; ++h) {
+                                float2 sacc = mul2(g[h * PPH], xk[h * PPH]);
+#pragma unroll
+                                for (int i = 1; i < PPH; ++i) sacc = fma2(g[h * PPH + i], xk[h * PPH + i], sacc);
+                                part[h][k] = sacc.x + sacc.y;
+                            }
                         }
-                    if (HPT == 1) {
+                    }
+                    if (nv != W) {
+#pragma unroll
+                        for (int h = 0; h < HPT; ++h)
+#pragma unroll
+                            for (int k = 0; k < W; ++k) part[h][k] = k < nv ? part[h][k] : 0.f;
+                    }
+                    if constexpr (HPT == 1) {
                         for (int off = 1; off < lanes_per_head; off <<= 1) {
 #pragma unroll
                             for (int k = 0; k < W; ++k) part[0][k] += __shfl_xor_sync(0xffffffffu, part[0][k], off);
@@ -182,15 +211,7 @@ __global__ void __launch_bounds__(32 * (1 + TileCfg<E, HPT, true>::NCW), 1)
                             for (int k = 0; k < W; ++k) o[h * W + k] = part[h][k];
                         store_n<E, NWV>(dw + (static_cast<size_t>(t) * p.G + head) * W, o);
                     }
-#pragma unroll
-                    for (int k = W - 1; k >= 1; --k)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) xw[k][q] = xw[k - 1][q];
                 }
-#pragma unroll
-                for (int k = W - 1; k >= 1; --k)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[k][q] = acc[k - 1][q];
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&hdr->empty[s]);

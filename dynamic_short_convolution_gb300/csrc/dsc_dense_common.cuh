@@ -18,18 +18,32 @@ namespace dsc {
 constexpr int kDC = 256;        // channels per tile
 constexpr int kMaxStages = 8;   // shared-memory ring depth cap
 
-// Tokens per tile (TT) and per consumer warp (RPW), by element type, filter
-// values per lane (HPT = heads per lane: 8 for H=1, 4 for H=2, 2 for H=4,
-// 1 for H>=8) and direction.  Chosen so a stage is 35-60 KB and 3-5 stages fit.
+// Tokens per tile (TT) and per consumer warp (RPW), by element type, heads
+// per lane (HPT: 8 for H=1, 4 for H=2, 2 for H=4, 1 for H>=8) and direction.
+// bf16 forward: 16 consumer warps, stages of 60-85 KB (2-3 in flight).  bf16
+// backward: 8 consumer warps with 4-8 tokens each, so the W-1 halo steps of
+// the dx ring stay a small share of the work.  fp32 halves the tokens.
 template <typename E, int HPT, bool BWD>
 struct TileCfg {
     static constexpr bool kBf16 = sizeof(E) == 2;
-    static constexpr int TT = BWD ? (kBf16 ? (HPT <= 2 ? 32 : 16) : (HPT <= 2 ? 16 : 8))
-                                  : (kBf16 ? (HPT == 1 ? 64 : HPT == 8 ? 16 : 32)
-                                           : (HPT == 1 ? 32 : HPT == 8 ? 8 : 16));
-    static constexpr int RPW = (TT >= 64) ? 8 : 4;
+    static constexpr int TTb = BWD ? (HPT == 1 ? 64 : 32) : (HPT == 1 ? 96 : HPT == 2 ? 64 : HPT == 4 ? 48 : 32);
+    static constexpr int RPWb = BWD ? (HPT == 1 ? 8 : 4) : (HPT == 1 ? 6 : HPT == 2 ? 4 : HPT == 4 ? 3 : 2);
+    static constexpr int TT = kBf16 ? TTb : (BWD && HPT == 8 ? 8 : TTb / 2);
+    static constexpr int RPW = kBf16 ? RPWb : (BWD ? (HPT == 1 ? 8 : 4) : RPWb);
     static constexpr int NCW = TT / RPW;  // consumer warps
+    static_assert(TT % RPW == 0, "whole warps per tile");
 };
+
+// Filter values of one lane's channel pairs: wp[i][k] = (w[head(2i), k], w[head(2i+1), k]).
+template <int HPT, int W>
+__device__ __forceinline__ void filter_pairs(const float (&wv)[HPT * W], float2 (&wp)[4][W])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+            wp[i][k] = make_float2(wv[((2 * i) * HPT / 8) * W + k], wv[((2 * i + 1) * HPT / 8) * W + k]);
+}
 
 // Host-side plan of one launch of the TMA path.
 struct DensePlan {

@@ -116,43 +116,37 @@ __global__ void __launch_bounds__(32 * (1 + TileCfg<E, HPT, false>::NCW), 1)
             const bool cvalid = c < p.D;
             E *y = reinterpret_cast<E *>(p.out0);
 
-            float xw[W][8];  // xw[k] = x at token (t - k)
+            // x window as a ring: the row of step r (token t0+r0+r) sits in slot ring(r, W)
+            float2 xw[W][4];
 #pragma unroll
-            for (int k = 1; k < W; ++k) load8(xs + (r0 + W - 1 - k) * kDC, xw[k]);
+            for (int r = -(W - 1); r < 0; ++r) load8x2(xs + (r0 + r + W - 1) * kDC, xw[ring(r, W)]);
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
                 const int j = r0 + r;  // tile-local token
-                load8(xs + (j + W - 1) * kDC, xw[0]);
+                load8x2(xs + (j + W - 1) * kDC, xw[ring(r, W)]);
                 float wv[NWV];
                 load_n<E, NWV>(ws + j * p.w_box, wv);
+                float2 wp[4][W];
+                filter_pairs<HPT, W>(wv, wp);
                 const int nv = nvs[j];
-                float out[8];
+                float2 out[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) out[i] = xw[ring(r, W)][i];  // residual
                 if (nv == W) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int hq = (q * HPT) / 8;  // this channel's head within the lane's slice
-                        float acc = xw[0][q];
+                    for (int k = 0; k < W; ++k)
 #pragma unroll
-                        for (int k = 0; k < W; ++k) acc = fmaf(wv[hq * W + k], xw[k][q], acc);
-                        out[q] = acc;
-                    }
+                        for (int i = 0; i < 4; ++i) out[i] = fma2(wp[i][k], xw[ring(r - k, W)][i], out[i]);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int hq = (q * HPT) / 8;
-                        float acc = xw[0][q];
+                    for (int k = 0; k < W; ++k)
+                        if (k < nv) {
 #pragma unroll
-                        for (int k = 0; k < W; ++k) acc = fmaf(wv[hq * W + k], k < nv ? xw[k][q] : 0.f, acc);
-                        out[q] = acc;
-                    }
+                            for (int i = 0; i < 4; ++i) out[i] = fma2(wp[i][k], xw[ring(r - k, W)][i], out[i]);
+                        }
                 }
                 const int t = t0 + j;
-                if (cvalid && t < p.BT) store8(y + static_cast<size_t>(t) * p.D + c, out);
-#pragma unroll
-                for (int k = W - 1; k >= 1; --k) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) xw[k][q] = xw[k - 1][q];
-                }
+                if (cvalid && t < p.BT) store8x2(y + static_cast<size_t>(t) * p.D + c, out);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&hdr->empty[s]);

@@ -172,6 +172,56 @@ __device__ __forceinline__ void load8(const float *p, float (&v)[8])
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// 8 consecutive elements as 4 channel pairs (fp32x2), for packed fp32 math.
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ void load8x2(const __nv_bfloat16 *p, float2 (&v)[4])
+{
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    v[0] = bf16x2_to_f2(u.x);
+    v[1] = bf16x2_to_f2(u.y);
+    v[2] = bf16x2_to_f2(u.z);
+    v[3] = bf16x2_to_f2(u.w);
+}
+
+__device__ __forceinline__ void load8x2(const float *p, float2 (&v)[4])
+{
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    v[0] = make_float2(a.x, a.y);
+    v[1] = make_float2(a.z, a.w);
+    v[2] = make_float2(b.x, b.y);
+    v[3] = make_float2(b.z, b.w);
+}
+
+__device__ __forceinline__ void store8x2(__nv_bfloat16 *p, const float2 (&v)[4])
+{
+    uint4 u;
+    __nv_bfloat162 h0 = __float22bfloat162_rn(v[0]), h1 = __float22bfloat162_rn(v[1]);
+    __nv_bfloat162 h2 = __float22bfloat162_rn(v[2]), h3 = __float22bfloat162_rn(v[3]);
+    u.x = *reinterpret_cast<uint32_t *>(&h0);
+    u.y = *reinterpret_cast<uint32_t *>(&h1);
+    u.z = *reinterpret_cast<uint32_t *>(&h2);
+    u.w = *reinterpret_cast<uint32_t *>(&h3);
+    *reinterpret_cast<uint4 *>(p) = u;
+}
+
+__device__ __forceinline__ void store8x2(float *p, const float2 (&v)[4])
+{
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+}
+
+// Packed fp32 fused multiply-add / multiply (two lanes per instruction on sm_100+).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+// Compile-time slot of a W-slot ring: ((i % W) + W) % W.
+__host__ __device__ constexpr int ring(int i, int W) { return ((i % W) + W) % W; }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
