@@ -21,13 +21,15 @@ constexpr int kMaxStages = 8;   // shared-memory ring depth cap
 // Tokens per tile (TT) and per consumer warp (RPW), by element type, heads
 // per lane (HPT: 8 for H=1, 4 for H=2, 2 for H=4, 1 for H>=8) and direction.
 // bf16 forward: 16 consumer warps, stages of 60-85 KB (2-3 in flight).  bf16
-// backward: 8 consumer warps with 4-8 tokens each, so the W-1 halo steps of
-// the dx ring stay a small share of the work.  fp32 halves the tokens.
+// backward: 16 consumer warps of 3 tokens for H >= 8 (stages of ~45 KB, 4 in
+// flight), 4 warps of 4 tokens for H = 1 (the filter rows dominate a stage).
+// Chosen by measured sweeps of the tile shape on GB300.  fp32 halves the tokens.
 template <typename E, int HPT, bool BWD>
 struct TileCfg {
     static constexpr bool kBf16 = sizeof(E) == 2;
-    static constexpr int TTb = BWD ? (HPT == 1 ? 64 : 32) : (HPT == 1 ? 96 : HPT == 2 ? 64 : HPT == 4 ? 48 : 32);
-    static constexpr int RPWb = BWD ? (HPT == 1 ? 8 : 4) : (HPT == 1 ? 6 : HPT == 2 ? 4 : HPT == 4 ? 3 : 2);
+    static constexpr int TTb = BWD ? (HPT == 1 ? 48 : HPT == 8 ? 16 : 32)
+                                   : (HPT == 1 ? 96 : HPT == 2 ? 64 : HPT == 4 ? 48 : 32);
+    static constexpr int RPWb = BWD ? (HPT == 1 ? 3 : 4) : (HPT == 1 ? 6 : HPT == 2 ? 4 : HPT == 4 ? 3 : 2);
     static constexpr int TT = kBf16 ? TTb : (BWD && HPT == 8 ? 8 : TTb / 2);
     static constexpr int RPW = kBf16 ? RPWb : (BWD ? (HPT == 1 ? 8 : 4) : RPWb);
     static constexpr int NCW = TT / RPW;  // consumer warps
@@ -70,8 +72,6 @@ inline int ilog2_exact(int v)
     while ((1 << s) < v) ++s;
     return (1 << s) == v ? s : -1;
 }
-
-inline unsigned align_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 
 // Decide whether the TMA path can take these arguments and lay out its stages.
 // Returns false (use the scalar path) when a TMA alignment or size rule fails.

@@ -79,6 +79,8 @@ inline dsc_status launched(unsigned n = 1)
     return cuda_status(e);
 }
 
+inline unsigned align_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<unsigned long long>(p) & 15ull) == 0; }
 
 }  // namespace dsc
