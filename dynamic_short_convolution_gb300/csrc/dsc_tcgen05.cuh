@@ -51,13 +51,31 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: A and B bf16 (both
-// K-major), D fp32, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+// General shared-memory matrix descriptor: start address, leading and stride
+// byte offsets, swizzle mode (0 none, 2 128-byte, 4 64-byte, 6 32-byte).
+// K-major swizzled: SBO = distance between 8-row groups (LBO unused).
+// MN-major swizzled: rows are K indices holding 64 MN elements (128 B), SBO =
+// distance between groups of 8 K rows, LBO = distance between 64-wide MN blocks.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(swizzle & 7u) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: A and B bf16, D fp32,
+// shape M x N; a_mn / b_mn select the MN-major (transposed) operand layouts.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false, bool b_mn = false)
 {
     return (1u << 4)                                  // D format: fp32
            | (1u << 7)                                // A format: bf16
            | (1u << 10)                               // B format: bf16
+           | ((a_mn ? 1u : 0u) << 15)                 // A major-ness: 0 K-major, 1 MN-major
+           | ((b_mn ? 1u : 0u) << 16)                 // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }

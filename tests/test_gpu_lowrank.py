@@ -80,3 +80,70 @@ def test_lowrank_fwd_deterministic(dsc):
     a = dsc.dsc_lowrank_fwd(g["x"], g["z"], g["U"], g["bias"], cu_seqlens=g["cu_seqlens"])
     b = dsc.dsc_lowrank_fwd(g["x"], g["z"], g["U"], g["bias"], cu_seqlens=g["cu_seqlens"])
     assert torch.equal(a, b)
+
+
+# backward: R a multiple of 16, at most 64
+SMALL_BWD = [
+    (2, 300, 256, 4, 64, True),
+    (1, 130, 128, 4, 16, False),
+    (2, 77, 192, 3, 32, True),
+    (1, 200, 64, 5, 48, True),
+    (1, 129, 256, 8, 64, False),
+    (2, 50, 512, 2, 16, True),
+    (1, 260, 200, 4, 64, True),
+    (1, 64, 64, 1, 64, False),
+    (3, 3, 64, 4, 64, False),
+    (2, 140, 96, 6, 32, True),
+    (1, 257, 136, 7, 48, True),
+    (2, 260, 2048, 4, 64, True),
+]
+
+
+def _bwd_check(dsc, oracle_mod, wl, rows=None, cols=None):
+    d = inputs.make(wl)
+    g = _dev(d)
+    dx, dz, dU, db = dsc.dsc_lowrank_bwd(g["x"], g["z"], g["U"], g["bias"], g["dy"], cu_seqlens=g["cu_seqlens"])
+    assert dsc.dsc_sync_status() == dsc.DSC_OK
+    BT, D, R, NW = wl.B * wl.T, wl.D, wl.R, wl.D * wl.W
+    dx, dz = dx.reshape(BT, D), dz.reshape(BT, R)
+    for r0, r1 in (rows or [(0, BT)]):
+        ref = oracle_mod.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
+                                     rows=(r0, r1), want=("dx", "dz"))
+        assert_close(dx[r0:r1], ref["dx"], "bf16", f"dx rows {r0}:{r1}")
+        assert_close(dz[r0:r1], ref["dz"], "bf16", f"dz rows {r0}:{r1}")
+    c = np.arange(NW) if cols is None else np.asarray(cols)
+    ref = oracle_mod.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
+                                 cols=c, want=("dU", "db"))
+    assert_close(dU[:, c], ref["dU"], "bf16", "dU")
+    assert_close(db[c], ref["db"], "bf16", "db")
+    return dx, dz, dU, db
+
+
+@pytest.mark.parametrize("case", SMALL_BWD, ids=lambda c: "B{}T{}D{}W{}R{}{}".format(*c[:5], "p" if c[5] else ""))
+def test_lowrank_bwd_small(dsc, oracle_mod, case):
+    B, T, D, W, R, packed = case
+    wl = inputs.custom(B, T, D, W, R=R, dtype="bf16", seed_id=700 + zlib.crc32(repr(case).encode()) % 500,
+                       packed=packed, doc_min=1, doc_max=40)
+    _bwd_check(dsc, oracle_mod, wl)
+
+
+def test_lowrank_bwd_full_size_sampled(dsc, oracle_mod):
+    wl = inputs.WORKLOADS[4]
+    BT = wl.B * wl.T
+    rng = np.random.default_rng(5)
+    starts = sorted({0, 122, 125, BT - 4, wl.T - 2, *map(int, rng.integers(0, BT - 4, size=4))})
+    rows = [(s, min(s + 4, BT)) for s in starts]
+    cols = sorted({0, 1, 255, 256, wl.D * wl.W - 1, *map(int, rng.integers(0, wl.D * wl.W, size=27))})
+    dx, dz, dU, db = _bwd_check(dsc, oracle_mod, wl, rows=rows, cols=cols)
+    for t in (dx, dz, dU, db):
+        assert torch.isfinite(t).all()
+
+
+def test_lowrank_bwd_deterministic_dx_and_close_repeat(dsc):
+    wl = inputs.custom(2, 300, 512, 4, R=64, dtype="bf16", seed_id=771, packed=True, doc_min=3, doc_max=50)
+    g = _dev(inputs.make(wl))
+    a = dsc.dsc_lowrank_bwd(g["x"], g["z"], g["U"], g["bias"], g["dy"], cu_seqlens=g["cu_seqlens"])
+    b = dsc.dsc_lowrank_bwd(g["x"], g["z"], g["U"], g["bias"], g["dy"], cu_seqlens=g["cu_seqlens"])
+    assert torch.equal(a[0], b[0])  # dx has a fixed summation order
+    for p_, q_ in zip(a[1:], b[1:]):  # dz, dU, db are sums of atomically added partials: order may vary
+        torch.testing.assert_close(p_.float(), q_.float(), rtol=1e-5, atol=1e-4)
