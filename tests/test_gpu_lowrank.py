@@ -145,5 +145,8 @@ def test_lowrank_bwd_deterministic_dx_and_close_repeat(dsc):
     a = dsc.dsc_lowrank_bwd(g["x"], g["z"], g["U"], g["bias"], g["dy"], cu_seqlens=g["cu_seqlens"])
     b = dsc.dsc_lowrank_bwd(g["x"], g["z"], g["U"], g["bias"], g["dy"], cu_seqlens=g["cu_seqlens"])
     assert torch.equal(a[0], b[0])  # dx has a fixed summation order
-    for p_, q_ in zip(a[1:], b[1:]):  # dz, dU, db are sums of atomically added partials: order may vary
-        torch.testing.assert_close(p_.float(), q_.float(), rtol=1e-5, atol=1e-4)
+    # dz, dU, db are sums of atomically added fp32 partials whose order may vary: dU and db agree to fp32
+    # rounding, and dz (rounded to bf16 afterwards) to one bf16 unit in the last place
+    torch.testing.assert_close(a[1].float(), b[1].float(), rtol=2 ** -7, atol=1e-3)
+    for p_, q_ in zip(a[2:], b[2:]):
+        torch.testing.assert_close(p_, q_, rtol=1e-5, atol=1e-4)
