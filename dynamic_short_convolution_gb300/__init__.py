@@ -25,6 +25,7 @@ from ._abi import (  # noqa: F401
     dsc_fwd,
     dsc_launch_count,
     dsc_lowrank_bwd,
+    dsc_lowrank_bwd_noalloc,
     dsc_lowrank_bwd_workspace_bytes,
     dsc_lowrank_fwd,
     dsc_sync_status,

@@ -34,6 +34,8 @@ SIGNATURES = {
     "dsc_lowrank_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "dsc_lowrank_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i,
                              _vp]),
+    "dsc_lowrank_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i,
+                                     _vp]),
     "dsc_validate_cu_seqlens": (_i, [_vp, _i, _i, _i, _vp]),
     "dsc_sync_status": (_i, [_vp]),
     "dsc_test_wait_timeout": (_i, [_u64, _vp]),
@@ -177,6 +179,28 @@ def dsc_lowrank_bwd(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=None, works
                               _dev(dz, "dz", x.dtype), _dev(dU, "dU", torch.float32),
                               _dev(db, "db", torch.float32), ws, B, T, D, W, R, _dt(x), cu, n, _stream(stream))
     _check(s, "dsc_lowrank_bwd")
+    return dx, dz, dU, db
+
+
+def dsc_lowrank_bwd_noalloc(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=None, *, cu_seqlens=None,
+                            stream=None):
+    """dsc_lowrank_bwd without a caller workspace, for callers that cannot allocate device memory for one:
+    the library's own fixed 8 MiB device array holds the partial sums (B*T*R <= 2,097,152; calls that
+    overlap on the GPU race on it).  The output tensors, when not given, are allocated here by torch."""
+    B, T, D = x.shape
+    R = z.shape[-1]
+    W = U.shape[1] // D
+    dx = torch.empty_like(x) if dx is None else dx
+    dz = torch.empty_like(z) if dz is None else dz
+    dU = torch.empty(U.shape, dtype=torch.float32, device=x.device) if dU is None else dU
+    db = torch.empty(bias.shape, dtype=torch.float32, device=x.device) if db is None else db
+    cu, n = _cu(cu_seqlens)
+    s = lib().dsc_lowrank_bwd_noalloc(_dev(x, "x"), _dev(z, "z", x.dtype), _dev(U, "U", x.dtype),
+                                      _dev(bias, "bias", torch.float32), _dev(dy, "dy", x.dtype),
+                                      _dev(dx, "dx", x.dtype), _dev(dz, "dz", x.dtype),
+                                      _dev(dU, "dU", torch.float32), _dev(db, "db", torch.float32), B, T, D, W, R,
+                                      _dt(x), cu, n, _stream(stream))
+    _check(s, "dsc_lowrank_bwd_noalloc")
     return dx, dz, dU, db
 
 

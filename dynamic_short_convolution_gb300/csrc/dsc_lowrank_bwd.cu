@@ -26,6 +26,8 @@
 // Row exchange for dx: the tap-k term of token t lands on token t-k, which is
 // another TMEM lane: warp shuffles inside a warp, a small shared edge buffer
 // across the four lane quadrants.
+#include <mutex>
+
 #include "dsc_internal.h"
 #include "dsc_tcgen05.cuh"
 
@@ -691,4 +693,45 @@ dsc_status lowrank_bwd(const LowrankArgs &a)
     }
 }
 
+// ------------------------------------------------------------------ allocation-free entry point
+//
+// Some callers cannot allocate device memory for the workspace: a plugin inside
+// a host framework that owns the whole device memory pool under a fixed memory
+// plan, or a latency-critical loop that must never enter the allocator.  For
+// them, dsc_lowrank_bwd_noalloc takes its fp32 dz partial sums from the
+// fixed-size array below, which lives in the library's static device memory
+// (every GPU that loads the library holds it until the process exits).
+
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 21;  // 8 MiB: B*T*R <= 2,097,152
+static __device__ __align__(256) float g_lrb_scratch[kNoAllocScratchFloats];
+
+// Device address of g_lrb_scratch on the current device, looked up once per
+// device (host code may not use the symbol itself as an address).
+static float *noalloc_scratch()
+{
+    static std::mutex mu;
+    static float *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_lrb_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<float *>(ptr);
+    }
+    return addr[dev];
+}
+
 }  // namespace dsc
+
+extern "C" dsc_status dsc_lowrank_bwd_noalloc(const void *x, const void *z, const void *U, const float *bias,
+                                              const void *dy, void *dx, void *dz, float *dU, float *db, int B, int T,
+                                              int D, int W, int R, dsc_dtype dt, const int32_t *cu_seqlens,
+                                              int n_docs, cudaStream_t stream)
+{
+    if (B < 1 || T < 1 || R < 1) return DSC_ERR_INVALID_ARG;
+    if (static_cast<size_t>(B) * T * R > dsc::kNoAllocScratchFloats) return DSC_ERR_INVALID_ARG;  // beyond the array
+    float *scratch = dsc::noalloc_scratch();
+    if (!scratch) return DSC_ERR_CUDA;
+    return dsc_lowrank_bwd(x, z, U, bias, dy, dx, dz, dU, db, scratch, B, T, D, W, R, dt, cu_seqlens, n_docs, stream);
+}

@@ -139,6 +139,29 @@ dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const fl
                            dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
 
 /*
+ * dsc_lowrank_bwd_noalloc -- dsc_lowrank_bwd for callers that cannot allocate
+ * device memory: a plugin inside a host framework that owns the whole device
+ * memory pool under a fixed memory plan, or a latency-critical loop that must
+ * never enter the allocator.  The paper has no counterpart; this is an
+ * interface convenience.  Same arguments and results as dsc_lowrank_bwd,
+ * without `workspace`: the fp32 partial sums go to a fixed array of 8 MiB in
+ * the library's static device memory, held by every GPU that loads the
+ * library until the process exits.  Nothing is allocated or freed by the
+ * call, and no allocating library routine is used.
+ *   Limit: B*T*R <= 2,097,152 (the array holds that many fp32 values);
+ *   larger sizes return DSC_ERR_INVALID_ARG before anything is launched.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   Every call uses the same array and leaves its last contents there; the
+ *   call clears what must start at zero itself.  Calls that overlap on the GPU
+ *   (for example on two streams) race on the array: serialise them.
+ */
+dsc_status dsc_lowrank_bwd_noalloc(const void *x, const void *z, const void *U, const float *bias, const void *dy,
+                                   void *dx, void *dz, float *dU, float *db, int B, int T, int D, int W, int R,
+                                   dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
+
+/*
  * dsc_validate_cu_seqlens -- device-side check of packed-document offsets:
  * cu[0] == 0, strictly increasing, cu[n_docs] == B*T.  Asynchronous; a
  * violation is recorded as DSC_ERR_INVALID_ARG in the device status word,
