@@ -14,9 +14,13 @@
 //               its (W-1)-token causal halo; per-token valid-tap counts
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma (M=128, N=NB, K=16 per
 //               instruction) into one of two TMEM accumulators
-//   warps 2..9  epilogue: tcgen05.ld of the accumulator row of one token,
+//   warps 2..17 epilogue: tcgen05.ld of the accumulator row of one token,
 //               + bias, times the x window from shared memory, + residual,
 //               bf16 into a swizzled staging tile that one thread TMA-stores
+// Inside each group of 8 channels the filter columns are kept tap-major
+// (MMA column g*8W + k*8 + c for channel g*8+c, tap k): the 8 channels of one
+// tap are adjacent accumulator columns, so channel pairs feed packed fp32x2
+// math straight from TMEM registers.
 #include "dsc_internal.h"
 #include "dsc_tcgen05.cuh"
 
@@ -25,7 +29,7 @@ namespace dsc {
 namespace lrf {
 
 constexpr int kM = 128;            // tokens per tile (MMA M, TMEM lanes)
-constexpr int kEpiWarps = 8;       // two per TMEM lane quadrant
+constexpr int kEpiWarps = 16;      // four per TMEM lane quadrant
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kMaxStages = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
@@ -73,7 +77,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     constexpr int RB = CB * 2;         // bytes per x / y tile row
     constexpr int XR = kM + W - 1;     // x rows per tile
     constexpr int GROUPS = CB / 8;     // 8-channel groups per block
-    constexpr int GPH = GROUPS / 2;    // groups per epilogue half
+    constexpr int GPW = GROUPS / 4;    // groups per epilogue warp (four warps per lane quadrant)
     static_assert(NB % 16 == 0 && NB <= 256, "MMA N");
     constexpr uint32_t IDESC = idesc_bf16_f32(kM, NB);
 
@@ -86,6 +90,11 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     float *b_s = reinterpret_cast<float *>(base + p.b_off);  // [NB]
     uint8_t *stages = base + p.st_off;
 
+    // block column n = (g*8 + c)*W + k  ->  MMA column g*8W + k*8 + c
+    auto tap_major = [](int n) {
+        const int g = n / (8 * W), rem = n - g * (8 * W);
+        return g * (8 * W) + (rem % W) * 8 + rem / W;
+    };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nstages; ++s) {
@@ -135,13 +144,13 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 const int a = r >> 6, c = (r & 63) >> 3, o = (r & 7) * 2;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int row = n + j;
+                    const int row = tap_major(n + j);  // MMA column of block column n+j
                     *reinterpret_cast<uint16_t *>(u_s + a * (NB * 128) + row * 128 + ((c ^ (row & 7)) << 4) + o) = e[j];
                 }
             }
             for (int n = threadIdx.x; n < NB; n += blockDim.x) {
                 const int gn = nb * NB + n;
-                b_s[n] = gn < p.N ? p.bias[gn] : 0.f;
+                b_s[tap_major(n)] = gn < p.N ? p.bias[gn] : 0.f;
             }
             fence_proxy_async_smem();
         }
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         } else {
             // ---------------- epilogue
             const int q = warp & 3;            // TMEM lane quadrant
-            const int h = (warp - 2) >> 2;     // which half of the channel groups
+            const int h = (warp - 2) >> 2;     // which quarter of the channel groups
             const int row = q * 32 + lane;     // token within the tile
             const bool store_thread = (threadIdx.x == 64);
             int i = it;
@@ -242,37 +251,47 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 const uint8_t *st = stages + s * p.stage_bytes;
                 const uint8_t *xs = st + p.x_off_in_stage;
                 const int nv = reinterpret_cast<const int8_t *>(st + p.nv_off_in_stage)[row];
+                const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
                 uint8_t *ys = y_s + (i & 1) * (kM * RB);
                 const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
 #pragma unroll
-                for (int gi = 0; gi < GPH; ++gi) {
-                    const int g = h * GPH + gi;  // 8-channel group
-                    uint32_t acc[8 * W];
+                for (int gi = 0; gi < GPW; ++gi) {
+                    const int g = h * GPW + gi;  // 8-channel group
+                    uint32_t acc[8 * W];         // acc[k*8 + c]: tap k of channel g*8 + c
                     tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
-                    float2 xk[W][4];
-#pragma unroll
-                    for (int k = 0; k < W; ++k) {  // x~ of token t-k: zero before the document start
-                        const int xr = row + (W - 1) - k;
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(xr, g));
-                        const bool on = k < nv;
-                        xk[k][0] = on ? bf16x2_to_f2(raw.x) : make_float2(0.f, 0.f);
-                        xk[k][1] = on ? bf16x2_to_f2(raw.y) : make_float2(0.f, 0.f);
-                        xk[k][2] = on ? bf16x2_to_f2(raw.z) : make_float2(0.f, 0.f);
-                        xk[k][3] = on ? bf16x2_to_f2(raw.w) : make_float2(0.f, 0.f);
+                    const float2 *bb = reinterpret_cast<const float2 *>(b_s + g * 8 * W);
+                    float2 out[4];
+                    {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + W - 1, g));
+                        out[0] = bf16x2_to_f2(raw.x);  // residual: x of the token itself
+                        out[1] = bf16x2_to_f2(raw.y);
+                        out[2] = bf16x2_to_f2(raw.z);
+                        out[3] = bf16x2_to_f2(raw.w);
                     }
                     tmem_ld_wait();
-                    float2 out[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) out[e] = xk[0][e];
-                    const float *bb = b_s + g * 8 * W;
 #pragma unroll
                     for (int k = 0; k < W; ++k) {
+                        float2 xk[4];
+                        if (k == 0) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) xk[e] = out[e];
+                        } else {
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
+                            xk[0] = bf16x2_to_f2(raw.x);
+                            xk[1] = bf16x2_to_f2(raw.y);
+                            xk[2] = bf16x2_to_f2(raw.z);
+                            xk[3] = bf16x2_to_f2(raw.w);
+                            if (!full_taps && k >= nv) {  // x~ is zero before the document start
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) xk[e] = make_float2(0.f, 0.f);
+                            }
+                        }
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int c0 = 2 * e, c1 = 2 * e + 1;  // channel pair within the group
-                            const float2 wk = make_float2(__uint_as_float(acc[c0 * W + k]) + bb[c0 * W + k],
-                                                          __uint_as_float(acc[c1 * W + k]) + bb[c1 * W + k]);
-                            out[e] = fma2(wk, xk[k][e], out[e]);
+                            const float2 wk = __fadd2_rn(
+                                make_float2(__uint_as_float(acc[k * 8 + 2 * e]), __uint_as_float(acc[k * 8 + 2 * e + 1])),
+                                bb[k * 4 + e]);
+                            out[e] = fma2(wk, xk[e], out[e]);
                         }
                     }
                     uint4 o;
