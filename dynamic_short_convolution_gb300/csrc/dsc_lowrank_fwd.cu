@@ -30,7 +30,8 @@ namespace lrf {
 
 constexpr int kM = 128;            // tokens per tile (MMA M, TMEM lanes)
 constexpr int kEpiWarps = 16;      // four per TMEM lane quadrant
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiWarp0 = 3;       // warps 0..2: producer, MMA issuer, storer
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kMaxStages = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
 
@@ -42,7 +43,7 @@ struct Params {
     int BT, T, D, R, N;            // N = D * W filter columns
     int n_nb, n_mt, n_units;
     int ksteps, kchunks;           // MMA K steps of 16; 64-wide K chunks
-    unsigned u_off, y_off, b_off, st_off, stage_bytes, z_bytes, x_bytes, x_off_in_stage, nv_off_in_stage;
+    unsigned u_off, bt_off, one_off, y_off, st_off, stage_bytes, z_bytes, x_bytes, x_off_in_stage, nv_off_in_stage;
     int nstages;
     int *status;
     unsigned long long wait_ns;
@@ -53,6 +54,8 @@ struct Header {
     uint64_t empty[kMaxStages];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
+    uint64_t y_full[2];
+    uint64_t y_empty[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -75,7 +78,6 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     using namespace lrf;
     constexpr int NB = CB * W;         // filter columns per block (MMA N)
     constexpr int RB = CB * 2;         // bytes per x / y tile row
-    constexpr int XR = kM + W - 1;     // x rows per tile
     constexpr int GROUPS = CB / 8;     // 8-channel groups per block
     constexpr int GPW = GROUPS / 4;    // groups per epilogue warp (four warps per lane quadrant)
     static_assert(NB % 16 == 0 && NB <= 256, "MMA N");
@@ -85,12 +87,13 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     Header *hdr = reinterpret_cast<Header *>(smem_raw);
     uint8_t *base = smem_raw + 1024;
     base += (1024u - (smem_u32(base) & 1023u)) & 1023u;
-    uint8_t *u_s = base + p.u_off;                           // [kchunks][NB rows][128 B], swizzled
-    uint8_t *y_s = base + p.y_off;                           // 2 x [kM rows][RB], swizzled
-    float *b_s = reinterpret_cast<float *>(base + p.b_off);  // [NB]
+    uint8_t *u_s = base + p.u_off;       // [kchunks][NB rows][128 B], 128-B swizzled, K-major
+    uint8_t *bt_s = base + p.bt_off;     // bias as an MMA B tile: [NB rows][16 K], no swizzle
+    uint8_t *one_s = base + p.one_off;   // all-ones MMA A tile [128 rows][16 K]
+    uint8_t *y_s = base + p.y_off;       // 2 x [kM rows][RB], swizzled
     uint8_t *stages = base + p.st_off;
 
-    // block column n = (g*8 + c)*W + k  ->  MMA column g*8W + k*8 + c
+    // block column n = (g*8 + c)*W + k  ->  MMA column g*8W + k*8 + c (tap-major inside a group)
     auto tap_major = [](int n) {
         const int g = n / (8 * W), rem = n - g * (8 * W);
         return g * (8 * W) + (rem % W) * 8 + rem / W;
@@ -104,10 +107,14 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&hdr->tmem_full[b], 1);
             mbar_init(&hdr->tmem_empty[b], kEpiWarps);
+            mbar_init(&hdr->y_full[b], kEpiWarps);
+            mbar_init(&hdr->y_empty[b], 1);
         }
         hdr->abort_flag = 0;
         fence_mbarrier_init();
     }
+    for (int i = threadIdx.x; i < kM * 16 / 2; i += blockDim.x)
+        reinterpret_cast<uint32_t *>(one_s)[i] = 0x3F803F80u;  // bf16 1.0 pairs
     if (warp == 1) {
         tmem_alloc(&hdr->tmem_base, kTmemCols);
         tmem_relinquish();
@@ -131,7 +138,8 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         const int nb = u / p.n_mt;
         const int seg_end = min(u_end, (nb + 1) * p.n_mt);
 
-        // ---- the block's filter generator: U[:, nb*NB .. +NB) transposed to K-major, and its bias
+        // ---- the block's filter generator: U[:, nb*NB .. +NB) transposed to K-major, and the bias
+        //      as an extra K step (exact bf16 hi + lo pair) that the all-ones A tile adds in
         {
             const int nK = p.kchunks * 64;
             const int items = nK * (NB / 8);
@@ -150,7 +158,15 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             }
             for (int n = threadIdx.x; n < NB; n += blockDim.x) {
                 const int gn = nb * NB + n;
-                b_s[tap_major(n)] = gn < p.N ? p.bias[gn] : 0.f;
+                const float bv = gn < p.N ? p.bias[gn] : 0.f;
+                const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv)));
+                const uint32_t lo =
+                    static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv - __uint_as_float(hi << 16))));
+                const int row = tap_major(n);
+                // core matrices of 8 rows x 16 B: K-half 0 at ((row/8)*2)*128, K-half 1 next to it
+                uint8_t *cm = bt_s + ((row >> 3) * 2) * 128 + (row & 7) * 16;
+                *reinterpret_cast<uint4 *>(cm) = make_uint4(hi | (lo << 16), 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(cm + 128) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
         }
@@ -188,7 +204,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 }
             }
         } else if (warp == 1) {
-            // ---------------- MMA issuer
+            // ---------------- MMA issuer: acc = z . U_blk (K = R), then += 1 . bias
             int i = it;
             for (int v = u; v < seg_end; ++v, ++i) {
                 const int s = i % p.nstages;
@@ -215,30 +231,51 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                         const uint64_t bd = sdesc_kmajor_sw128(us + a * (NB * 128) + kk * 32);
                         umma_bf16(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
                     }
+                    umma_bf16(d, sdesc(smem_u32(one_s), 128, 256, 0), sdesc(smem_u32(bt_s), 128, 256, 0), IDESC, 1u);
                     umma_commit(&hdr->empty[s]);
                     umma_commit(&hdr->tmem_full[b]);
                     mma_last = i;
                 }
                 __syncwarp();
             }
+        } else if (warp == 2) {
+            // ---------------- storer: one TMA store per finished y tile, then frees its staging buffer
+            int i = it;
+            for (int v = u; v < seg_end; ++v, ++i) {
+                const int yb = i & 1;
+                bool ok = mbar_wait(&hdr->y_full[yb], (i >> 1) & 1, p.wait_ns);
+                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        record_status(p.status, kStatusTimeout);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
+                if (lane == 0) {
+                    const int t0 = (v - nb * p.n_mt) * kM;
+                    tma_store_2d(&tm_y, y_s + yb * (kM * RB), nb * CB, t0);
+                    tma_store_commit();
+                    tma_store_wait_read<1>();  // the store of tile i-1 has left its staging buffer
+                    if (i > 0) mbar_arrive(&hdr->y_empty[yb ^ 1]);
+                }
+                __syncwarp();
+            }
         } else {
-            // ---------------- epilogue
-            const int q = warp & 3;            // TMEM lane quadrant
-            const int h = (warp - 2) >> 2;     // which quarter of the channel groups
-            const int row = q * 32 + lane;     // token within the tile
-            const bool store_thread = (threadIdx.x == 64);
+            // ---------------- epilogue: y = x + sum_k acc_k * x~_k (the bias is inside acc)
+            const int q = warp & 3;                          // TMEM lane quadrant
+            const int h = (warp - kEpiWarp0) >> 2;           // which quarter of the channel groups
+            const int row = q * 32 + lane;                   // token within the tile
             int i = it;
             for (int v = u; v < seg_end; ++v, ++i) {
                 const int s = i % p.nstages;
                 const uint32_t ph = (i / p.nstages) & 1;
                 const int b = i & 1;
                 const uint32_t tph = (i >> 1) & 1;
-                bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns);
-                ok = ok && (*abort_flag == 0);
-                // the staging buffer of this parity was last read by the store issued two tiles ago
-                if (store_thread) tma_store_wait_read<1>();
-                // one decision for all epilogue warps: none may wait alone at a later barrier
-                if (named_bar_any(1, 32 * kEpiWarps, !ok)) {
+                bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns) &&
+                          mbar_wait(&hdr->y_empty[b], tph ^ 1, p.wait_ns);
+                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+                if (!ok) {
                     if (lane == 0) {
                         record_status(p.status, kStatusTimeout);
                         *abort_flag = 1;
@@ -246,20 +283,17 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const int mt = v - nb * p.n_mt;
-                const int t0 = mt * kM;
                 const uint8_t *st = stages + s * p.stage_bytes;
                 const uint8_t *xs = st + p.x_off_in_stage;
                 const int nv = reinterpret_cast<const int8_t *>(st + p.nv_off_in_stage)[row];
                 const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
-                uint8_t *ys = y_s + (i & 1) * (kM * RB);
+                uint8_t *ys = y_s + b * (kM * RB);
                 const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
 #pragma unroll
                 for (int gi = 0; gi < GPW; ++gi) {
                     const int g = h * GPW + gi;  // 8-channel group
                     uint32_t acc[8 * W];         // acc[k*8 + c]: tap k of channel g*8 + c
                     tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
-                    const float2 *bb = reinterpret_cast<const float2 *>(b_s + g * 8 * W);
                     float2 out[4];
                     {
                         const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + W - 1, g));
@@ -268,13 +302,14 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                         out[2] = bf16x2_to_f2(raw.z);
                         out[3] = bf16x2_to_f2(raw.w);
                     }
+                    const float2 x0[4] = {out[0], out[1], out[2], out[3]};
                     tmem_ld_wait();
 #pragma unroll
                     for (int k = 0; k < W; ++k) {
                         float2 xk[4];
                         if (k == 0) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) xk[e] = out[e];
+                            for (int e = 0; e < 4; ++e) xk[e] = x0[e];
                         } else {
                             const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
                             xk[0] = bf16x2_to_f2(raw.x);
@@ -287,12 +322,10 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                             }
                         }
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 wk = __fadd2_rn(
-                                make_float2(__uint_as_float(acc[k * 8 + 2 * e]), __uint_as_float(acc[k * 8 + 2 * e + 1])),
-                                bb[k * 4 + e]);
-                            out[e] = fma2(wk, xk[e], out[e]);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            out[e] = fma2(make_float2(__uint_as_float(acc[k * 8 + 2 * e]),
+                                                      __uint_as_float(acc[k * 8 + 2 * e + 1])),
+                                          xk[e], out[e]);
                     }
                     uint4 o;
                     __nv_bfloat162 h0 = __float22bfloat162_rn(out[0]), h1 = __float22bfloat162_rn(out[1]);
@@ -303,18 +336,14 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     o.w = *reinterpret_cast<uint32_t *>(&h3);
                     *reinterpret_cast<uint4 *>(ys + swz<RB>(row, g)) = o;
                 }
-                // accumulator and x tile fully read: release them
+                // accumulator and x tile read; y written: hand them on
                 tc_fence_before();
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&hdr->tmem_empty[b]);
                     mbar_arrive(&hdr->empty[s]);
-                }
-                fence_proxy_async_smem();
-                named_bar(1, 32 * kEpiWarps);
-                if (store_thread) {
-                    tma_store_2d(&tm_y, ys, nb * CB, t0);
-                    tma_store_commit();
+                    mbar_arrive(&hdr->y_full[b]);
                 }
             }
         }
@@ -331,7 +360,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     }
     if (warp == 1 && lane == 0 && mma_last >= 0)
         (void)mbar_wait(&hdr->tmem_full[mma_last & 1], (mma_last >> 1) & 1, kDrainLimitNs);
-    if (threadIdx.x == 64) tma_store_wait_all<0>();
+    if (warp == 2 && lane == 0) tma_store_wait_all<0>();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -362,14 +391,16 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     p.n_units = static_cast<int>(units);
     p.ksteps = (a.R + 15) / 16;
     p.kchunks = (a.R + 63) / 64;
-    // shared memory: [header 1 KB][align slack 1 KB][U][y staging x2][bias][stages]
+    // shared memory: [header 1 KB][align slack 1 KB][U][bias tile][ones tile][y staging x2][stages]
     unsigned off = 0;
     p.u_off = off;
     off += p.kchunks * NB * 128;
+    p.bt_off = align_up(off, 1024);
+    off = p.bt_off + NB * 32;
+    p.one_off = align_up(off, 1024);
+    off = p.one_off + kM * 32;
     p.y_off = align_up(off, 1024);
     off = p.y_off + 2 * kM * RB;
-    p.b_off = align_up(off, 1024);
-    off = p.b_off + NB * 4;
     p.st_off = align_up(off, 1024);
     p.z_bytes = p.kchunks * 16384;
     p.x_off_in_stage = p.z_bytes;
