@@ -30,7 +30,7 @@ namespace lrf {
 
 constexpr int kM = 128;            // tokens per tile (MMA M, TMEM lanes)
 constexpr int kEpiWarps = 16;      // four per TMEM lane quadrant
-constexpr int kEpiWarp0 = 3;       // warps 0..2: producer, MMA issuer, storer
+constexpr int kEpiWarp0 = 2;       // warps 0, 1: producer, MMA issuer
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kMaxStages = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
@@ -54,8 +54,6 @@ struct Header {
     uint64_t empty[kMaxStages];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t y_full[2];
-    uint64_t y_empty[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -90,7 +88,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     uint8_t *u_s = base + p.u_off;       // [kchunks][NB rows][128 B], 128-B swizzled, K-major
     uint8_t *bt_s = base + p.bt_off;     // bias as an MMA B tile: [NB rows][16 K], no swizzle
     uint8_t *one_s = base + p.one_off;   // all-ones MMA A tile [128 rows][16 K]
-    uint8_t *y_s = base + p.y_off;       // 2 x [kM rows][RB], swizzled
+    uint8_t *y_s = base + p.y_off;       // per epilogue warp: 2 x [32 rows][RB/4] staging for its own stores
     uint8_t *stages = base + p.st_off;
 
     // block column n = (g*8 + c)*W + k  ->  MMA column g*8W + k*8 + c (tap-major inside a group)
@@ -107,8 +105,6 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&hdr->tmem_full[b], 1);
             mbar_init(&hdr->tmem_empty[b], kEpiWarps);
-            mbar_init(&hdr->y_full[b], kEpiWarps);
-            mbar_init(&hdr->y_empty[b], 1);
         }
         hdr->abort_flag = 0;
         fence_mbarrier_init();
@@ -238,42 +234,21 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 }
                 __syncwarp();
             }
-        } else if (warp == 2) {
-            // ---------------- storer: one TMA store per finished y tile, then frees its staging buffer
-            int i = it;
-            for (int v = u; v < seg_end; ++v, ++i) {
-                const int yb = i & 1;
-                bool ok = mbar_wait(&hdr->y_full[yb], (i >> 1) & 1, p.wait_ns);
-                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        record_status(p.status, kStatusTimeout);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-                if (lane == 0) {
-                    const int t0 = (v - nb * p.n_mt) * kM;
-                    tma_store_2d(&tm_y, y_s + yb * (kM * RB), nb * CB, t0);
-                    tma_store_commit();
-                    tma_store_wait_read<1>();  // the store of tile i-1 has left its staging buffer
-                    if (i > 0) mbar_arrive(&hdr->y_empty[yb ^ 1]);
-                }
-                __syncwarp();
-            }
         } else {
-            // ---------------- epilogue: y = x + sum_k acc_k * x~_k (the bias is inside acc)
+            // ---------------- epilogue: y = x + sum_k acc_k * x~_k (the bias is inside acc).  Each warp
+            // owns 32 tokens x CB/4 channels of the tile and stores them itself (TMA, private double
+            // buffer), so no warp ever waits for another one.
             const int q = warp & 3;                          // TMEM lane quadrant
             const int h = (warp - kEpiWarp0) >> 2;           // which quarter of the channel groups
             const int row = q * 32 + lane;                   // token within the tile
+            uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * (RB / 4));
             int i = it;
             for (int v = u; v < seg_end; ++v, ++i) {
                 const int s = i % p.nstages;
                 const uint32_t ph = (i / p.nstages) & 1;
                 const int b = i & 1;
                 const uint32_t tph = (i >> 1) & 1;
-                bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns) &&
-                          mbar_wait(&hdr->y_empty[b], tph ^ 1, p.wait_ns);
+                bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
                 if (!ok) {
                     if (lane == 0) {
@@ -282,12 +257,14 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     }
                     break;
                 }
+                if (lane == 0) tma_store_wait_read<1>();  // this warp's store from two tiles ago has left buffer b
+                __syncwarp();
                 tc_fence_after();
                 const uint8_t *st = stages + s * p.stage_bytes;
                 const uint8_t *xs = st + p.x_off_in_stage;
                 const int nv = reinterpret_cast<const int8_t *>(st + p.nv_off_in_stage)[row];
                 const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
-                uint8_t *ys = y_s + b * (kM * RB);
+                uint8_t *ys = ywarp + b * (32 * (RB / 4));
                 const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
 #pragma unroll
                 for (int gi = 0; gi < GPW; ++gi) {
@@ -334,16 +311,18 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     o.y = *reinterpret_cast<uint32_t *>(&h1);
                     o.z = *reinterpret_cast<uint32_t *>(&h2);
                     o.w = *reinterpret_cast<uint32_t *>(&h3);
-                    *reinterpret_cast<uint4 *>(ys + swz<RB>(row, g)) = o;
+                    *reinterpret_cast<uint4 *>(ys + lane * (RB / 4) + gi * 16) = o;
                 }
-                // accumulator and x tile read; y written: hand them on
+                // accumulator and x tile read: hand them back; store this warp's y sub-tile
                 tc_fence_before();
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&hdr->tmem_empty[b]);
                     mbar_arrive(&hdr->empty[s]);
-                    mbar_arrive(&hdr->y_full[b]);
+                    const int t0 = (v - nb * p.n_mt) * kM;
+                    tma_store_2d(&tm_y, ys, nb * CB + h * (CB / 4), t0 + q * 32);
+                    tma_store_commit();
                 }
             }
         }
@@ -360,7 +339,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     }
     if (warp == 1 && lane == 0 && mma_last >= 0)
         (void)mbar_wait(&hdr->tmem_full[mma_last & 1], (mma_last >> 1) & 1, kDrainLimitNs);
-    if (warp == 2 && lane == 0) tma_store_wait_all<0>();
+    if (warp >= kEpiWarp0 && lane == 0) tma_store_wait_all<0>();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -400,7 +379,7 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     p.one_off = align_up(off, 1024);
     off = p.one_off + kM * 32;
     p.y_off = align_up(off, 1024);
-    off = p.y_off + 2 * kM * RB;
+    off = p.y_off + kEpiWarps * 2 * 32 * (RB / 4);
     p.st_off = align_up(off, 1024);
     p.z_bytes = p.kchunks * 16384;
     p.x_off_in_stage = p.z_bytes;
@@ -423,7 +402,7 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
         !encode_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.D, BT, static_cast<unsigned long long>(a.D) * 2,
                         CB, XR, sw) ||
         !encode_tmap_2d(&tm_y, a.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.D, BT, static_cast<unsigned long long>(a.D) * 2,
-                        CB, kM, sw))
+                        CB / 4, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
         return DSC_ERR_CUDA;
     auto kern = lowrank_fwd_tc<W, CB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
