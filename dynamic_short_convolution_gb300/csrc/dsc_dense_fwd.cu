@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(32 * (1 + TileCfg<E, HPT, false>::NCW), 1)
 #pragma unroll
         for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
         bool aborted = false;
+        DocCursor cursor;  // this CTA's tiles come in increasing token order
         int it = 0;
         for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++it) {
             const int s = it % p.nstages;
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(32 * (1 + TileCfg<E, HPT, false>::NCW), 1)
             int8_t *nv = reinterpret_cast<int8_t *>(st + p.nv_off);
             for (int r = lane; r < TT; r += 32) {
                 const int t = t0 + r;
-                nv[r] = static_cast<int8_t>(t < p.BT ? valid_taps(t, p.T, W, p.cu, p.n_docs) : W);
+                nv[r] = static_cast<int8_t>(t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W);
             }
             __syncwarp();
             if (lane == 0) {

@@ -318,21 +318,49 @@ __device__ __forceinline__ void store_n(E *p, const float (&v)[N])
 // Number of valid taps of token t (1..W): taps k with t-k inside t's document.
 // cu: packed-document offsets (n_docs + 1 entries) or nullptr.  Any content of
 // cu gives an in-range result, so malformed offsets cannot cause an
-// out-of-bounds access.
-__device__ __forceinline__ int valid_taps(long long t, int T, int W, const int32_t *cu, int n_docs)
+// out-of-bounds access.  (Token indices are < 2^31: 32-bit arithmetic.)
+__device__ __forceinline__ int valid_taps(int t, int T, int W, const int32_t *cu, int n_docs)
 {
-    long long ds = (t / T) * T;
+    int ds = t - t % T;  // start of t's sequence
     if (cu != nullptr) {
         int lo = 0, hi = n_docs;
         while (lo < hi) {  // largest i with cu[i] <= t
             const int mid = (lo + hi + 1) >> 1;
-            if ((long long)__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+            if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
         }
-        const long long c = __ldg(cu + lo);
+        const int c = __ldg(cu + lo);
         if (c <= t && c > ds) ds = c;
     }
-    long long nv = t - ds + 1;
-    return nv < 1 ? 1 : (nv > W ? W : (int)nv);
+    const int nv = t - ds + 1;
+    return nv < 1 ? 1 : (nv > W ? W : nv);
 }
+
+// valid_taps for a thread that asks about increasing tokens: it keeps the
+// index of the last document offset <= t and walks it forward (usually zero
+// or one step per token) instead of searching cu from scratch.  reset() when
+// the tokens jump backwards.  Same in-range guarantee for malformed offsets.
+struct DocCursor {
+    int ci = -1;
+    __device__ __forceinline__ void reset() { ci = -1; }
+    __device__ __forceinline__ int taps(int t, int T, int W, const int32_t *cu, int n_docs)
+    {
+        int ds = t - t % T;
+        if (cu != nullptr) {
+            if (ci < 0) {
+                int lo = 0, hi = n_docs;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+                }
+                ci = lo;
+            }
+            while (ci < n_docs && __ldg(cu + ci + 1) <= t) ++ci;
+            const int c = __ldg(cu + ci);
+            if (c <= t && c > ds) ds = c;
+        }
+        const int nv = t - ds + 1;
+        return nv < 1 ? 1 : (nv > W ? W : nv);
+    }
+};
 
 }  // namespace dsc

@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
 
         if (warp == 0) {
             // ---------------- producer: z, x (with the causal halo), dy tiles and valid-tap counts
+            DocCursor cursor;  // tokens increase within a run of tiles (the overlap rows repeat, never go back)
             for (int v = 0; v < ntiles; ++v) {
                 const int i = it + v;
                 const int s = i % kStages;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                 int8_t *nv = reinterpret_cast<int8_t *>(st + p.nv_in);
                 for (int r = lane; r < kM; r += 32) {
                     const int t = t0 + r;
-                    nv[r] = static_cast<int8_t>(t < p.BT ? valid_taps(t, p.T, W, p.cu, p.n_docs) : W);
+                    nv[r] = static_cast<int8_t>(t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W);
                 }
                 __syncwarp();
                 if (lane == 0) {

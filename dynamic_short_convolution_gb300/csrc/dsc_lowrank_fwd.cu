@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
 
         if (warp == 0) {
             // ---------------- producer
+            DocCursor cursor;  // tokens increase within a run of tiles
             int i = it;
             for (int v = u; v < seg_end; ++v, ++i) {
                 const int s = i % p.nstages;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 int8_t *nv = reinterpret_cast<int8_t *>(st + p.nv_off_in_stage);
                 for (int r = lane; r < kM; r += 32) {
                     const int t = t0 + r;
-                    nv[r] = static_cast<int8_t>(t < p.BT ? valid_taps(t, p.T, W, p.cu, p.n_docs) : W);
+                    nv[r] = static_cast<int8_t>(t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W);
                 }
                 __syncwarp();
                 if (lane == 0) {
