@@ -195,8 +195,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
         __syncthreads();
 
         if (warp == 0) {
-            // ---------------- producer: z, x (with the causal halo), dy tiles and valid-tap counts
-            DocCursor cursor;  // tokens increase within a run of tiles (the overlap rows repeat, never go back)
+            // ---------------- producer: z, x (with the causal halo) and dy tiles
             for (int v = 0; v < ntiles; ++v) {
                 const int i = it + v;
                 const int s = i % kStages;
@@ -213,12 +212,6 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                 const int mt = u + v - nb * p.n_mt;
                 const int t0 = mt * MS;
                 uint8_t *st = stages + s * p.stage_bytes;
-                int8_t *nv = reinterpret_cast<int8_t *>(st + p.nv_in);
-                for (int r = lane; r < kM; r += 32) {
-                    const int t = t0 + r;
-                    nv[r] = static_cast<int8_t>(t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W);
-                }
-                __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&hdr->full[s], p.z_bytes + p.x_bytes + p.dy_bytes);
                     tma_load_2d(st, &tm_z, &hdr->full[s], 0, t0);
@@ -309,6 +302,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
             const bool store_thread = (threadIdx.x == 64);
             int gcount = 0;  // groups processed (edge-buffer parity), equal across a half
             bool epi_abort = false;
+            DocCursor cursor;  // this thread's token increases from tile to tile within a run
             for (int v = 0; v < ntiles && !epi_abort; ++v) {
                 const int i = it + v;
                 const int s = i % kStages;
@@ -317,7 +311,6 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                 const uint8_t *st = stages + s * p.stage_bytes;
                 const uint8_t *xs = st + p.x_in;
                 const uint8_t *gys = st + p.dy_in;
-                const int8_t *nvs = reinterpret_cast<const int8_t *>(st + p.nv_in);
                 for (int j = 0; j < NSB && !epi_abort; ++j) {
                     const int step = i * NSB + j;
                     bool ok = mbar_wait(&hdr->accw_full, step & 1, p.wait_ns);
@@ -335,7 +328,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const int nv = nvs[row];
+                    const int nv = (t0 + row < p.BT) ? cursor.taps(t0 + row, p.T, W, p.cu, p.n_docs) : W;
                     uint32_t ghi[GPH][4 * W], glo[GPH][4 * W];
 #pragma unroll
                     for (int gi = 0; gi < GPH; ++gi) {

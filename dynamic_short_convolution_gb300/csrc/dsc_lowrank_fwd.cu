@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
 
         if (warp == 0) {
             // ---------------- producer
-            DocCursor cursor;  // tokens increase within a run of tiles
             int i = it;
             for (int v = u; v < seg_end; ++v, ++i) {
                 const int s = i % p.nstages;
@@ -187,12 +186,6 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 const int mt = v - nb * p.n_mt;
                 const int t0 = mt * kM;
                 uint8_t *st = stages + s * p.stage_bytes;
-                int8_t *nv = reinterpret_cast<int8_t *>(st + p.nv_off_in_stage);
-                for (int r = lane; r < kM; r += 32) {
-                    const int t = t0 + r;
-                    nv[r] = static_cast<int8_t>(t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W);
-                }
-                __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&hdr->full[s], p.z_bytes + p.x_bytes);
                     for (int a = 0; a < p.kchunks; ++a) tma_load_2d(st + a * 16384, &tm_z, &hdr->full[s], a * 64, t0);
@@ -243,6 +236,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             const int h = (warp - kEpiWarp0) >> 2;           // which quarter of the channel groups
             const int row = q * 32 + lane;                   // token within the tile
             uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * (RB / 4));
+            DocCursor cursor;  // this thread's token increases from tile to tile within a run
             int i = it;
             for (int v = u; v < seg_end; ++v, ++i) {
                 const int s = i % p.nstages;
@@ -263,7 +257,8 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 tc_fence_after();
                 const uint8_t *st = stages + s * p.stage_bytes;
                 const uint8_t *xs = st + p.x_off_in_stage;
-                const int nv = reinterpret_cast<const int8_t *>(st + p.nv_off_in_stage)[row];
+                const int t = (v - nb * p.n_mt) * kM + row;
+                const int nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;  // valid taps of this token
                 const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
                 uint8_t *ys = ywarp + b * (32 * (RB / 4));
                 const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
