@@ -139,36 +139,17 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         {
             const int nK = p.kchunks * 64;
             const int items = nK * (NB / 8);
-            // loads in batches of four per thread (one L2 round trip each), then the scattered smem stores
-            constexpr int kBatch = 4;
-            for (int m0 = 0; m0 * static_cast<int>(blockDim.x) < items; m0 += kBatch) {
-                uint4 vals[kBatch];
+            for (int idx = threadIdx.x; idx < items; idx += blockDim.x) {
+                const int n8 = idx / nK, r = idx - n8 * nK;
+                const int n = n8 * 8, gn = nb * NB + n;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (r < p.R && gn < p.N) v = *reinterpret_cast<const uint4 *>(p.U + static_cast<size_t>(r) * p.N + gn);
+                const uint16_t *e = reinterpret_cast<const uint16_t *>(&v);
+                const int a = r >> 6, c = (r & 63) >> 3, o = (r & 7) * 2;
 #pragma unroll
-                for (int m = 0; m < kBatch; ++m) {
-                    const int idx = threadIdx.x + (m0 + m) * blockDim.x;
-                    vals[m] = make_uint4(0u, 0u, 0u, 0u);
-                    if (idx < items) {
-                        const int n8 = idx / nK, r = idx - n8 * nK;
-                        const int gn = nb * NB + n8 * 8;
-                        if (r < p.R && gn < p.N)
-                            vals[m] = __ldg(reinterpret_cast<const uint4 *>(p.U + static_cast<size_t>(r) * p.N + gn));
-                    }
-                }
-#pragma unroll
-                for (int m = 0; m < kBatch; ++m) {
-                    const int idx = threadIdx.x + (m0 + m) * blockDim.x;
-                    if (idx < items) {
-                        const int n8 = idx / nK, r = idx - n8 * nK;
-                        const int n = n8 * 8;
-                        const uint16_t *e = reinterpret_cast<const uint16_t *>(&vals[m]);
-                        const int a = r >> 6, c = (r & 63) >> 3, o = (r & 7) * 2;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int row = tap_major(n + j);  // MMA column of block column n+j
-                            *reinterpret_cast<uint16_t *>(u_s + a * (NB * 128) + row * 128 + ((c ^ (row & 7)) << 4) + o) =
-                                e[j];
-                        }
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    const int row = tap_major(n + j);  // MMA column of block column n+j
+                    *reinterpret_cast<uint16_t *>(u_s + a * (NB * 128) + row * 128 + ((c ^ (row & 7)) << 4) + o) = e[j];
                 }
             }
             for (int n = threadIdx.x; n < NB; n += blockDim.x) {
@@ -281,37 +262,43 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
                 uint8_t *ys = ywarp + b * (32 * (RB / 4));
                 const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
-                uint32_t acc[GPW * 8 * W];  // acc[gi*8W + k*8 + c]: tap k of channel (h*GPW + gi)*8 + c
-                tmem_ld_cols<GPW * 8 * W>(trow + h * GPW * 8 * W, acc);
-                // the token's own x row of the first group is fetched while the TMEM load is in flight
-                uint4 x0 = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + W - 1, h * GPW));
-                tmem_ld_wait();
 #pragma unroll
                 for (int gi = 0; gi < GPW; ++gi) {
-                    const int g = h * GPW + gi;
-                    if (gi > 0) x0 = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + W - 1, g));
+                    const int g = h * GPW + gi;  // 8-channel group
+                    uint32_t acc[8 * W];         // acc[k*8 + c]: tap k of channel g*8 + c
+                    tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
                     float2 out[4];
-                    out[0] = bf16x2_to_f2(x0.x);  // residual: x of the token itself
-                    out[1] = bf16x2_to_f2(x0.y);
-                    out[2] = bf16x2_to_f2(x0.z);
-                    out[3] = bf16x2_to_f2(x0.w);
+                    {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + W - 1, g));
+                        out[0] = bf16x2_to_f2(raw.x);  // residual: x of the token itself
+                        out[1] = bf16x2_to_f2(raw.y);
+                        out[2] = bf16x2_to_f2(raw.z);
+                        out[3] = bf16x2_to_f2(raw.w);
+                    }
+                    const float2 x0[4] = {out[0], out[1], out[2], out[3]};
+                    tmem_ld_wait();
 #pragma unroll
                     for (int k = 0; k < W; ++k) {
-                        const uint4 xr = k == 0 ? x0 : *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
                         float2 xk[4];
-                        xk[0] = bf16x2_to_f2(xr.x);
-                        xk[1] = bf16x2_to_f2(xr.y);
-                        xk[2] = bf16x2_to_f2(xr.z);
-                        xk[3] = bf16x2_to_f2(xr.w);
-                        if (!full_taps && k >= nv) {  // x~ is zero before the document start
+                        if (k == 0) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) xk[e] = make_float2(0.f, 0.f);
+                            for (int e = 0; e < 4; ++e) xk[e] = x0[e];
+                        } else {
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
+                            xk[0] = bf16x2_to_f2(raw.x);
+                            xk[1] = bf16x2_to_f2(raw.y);
+                            xk[2] = bf16x2_to_f2(raw.z);
+                            xk[3] = bf16x2_to_f2(raw.w);
+                            if (!full_taps && k >= nv) {  // x~ is zero before the document start
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) xk[e] = make_float2(0.f, 0.f);
+                            }
                         }
-                        const uint32_t *ak = acc + gi * 8 * W + k * 8;
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            out[e] = fma2(make_float2(__uint_as_float(ak[2 * e]), __uint_as_float(ak[2 * e + 1])), xk[e],
-                                          out[e]);
+                            out[e] = fma2(make_float2(__uint_as_float(acc[k * 8 + 2 * e]),
+                                                      __uint_as_float(acc[k * 8 + 2 * e + 1])),
+                                          xk[e], out[e]);
                     }
                     uint4 o;
                     __nv_bfloat162 h0 = __float22bfloat162_rn(out[0]), h1 = __float22bfloat162_rn(out[1]);
