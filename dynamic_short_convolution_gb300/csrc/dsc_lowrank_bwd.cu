@@ -69,7 +69,7 @@ struct Params {
     float *db;
     int BT, T, D, R, N;
     int n_nb, n_mt, n_units, MS;
-    unsigned u_off, b_off, one_off, g_off, dx_off, e_off, st_off, stage_bytes;
+    unsigned u_off, bt_off, one_off, g_off, dx_off, e_off, st_off, stage_bytes;
     unsigned u_bytes, z_bytes, x_in, x_bytes, dy_in, dy_bytes, nv_in;
     int *status;
     unsigned long long wait_ns;
@@ -88,6 +88,12 @@ struct Header {
 };
 
 }  // namespace lrb
+
+// Four fp32 additions to global memory, no value returned.
+__device__ __forceinline__ void red_add_v4(float *dst, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
 
 template <int RB>
 __device__ __forceinline__ uint32_t swz_b(int row, int c)
@@ -128,8 +134,8 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
     uint8_t *base = smem_raw + 1024;
     base += (1024u - (smem_u32(base) & 1023u)) & 1023u;
     uint8_t *u_s = base + p.u_off;                            // [NSB][UCH][R rows][128 B]
-    float *b_s = reinterpret_cast<float *>(base + p.b_off);   // [NB]
-    uint8_t *one_s = base + p.one_off;                        // 1 KB of bf16 ones
+    uint8_t *bt_s = base + p.bt_off;                          // bias as MMA B tiles: [NSB][SNB rows][16 K], no swizzle
+    uint8_t *one_s = base + p.one_off;                        // 4 KB of bf16 ones (an MMA A tile of 128 x 16)
     uint8_t *g_s = base + p.g_off;                            // [2 (hi, lo)][2 chunks][128 rows][128 B]
     uint8_t *dx_s = base + p.dx_off;                          // [128 rows][RB], swizzled
     float2 *edge = reinterpret_cast<float2 *>(base + p.e_off);
@@ -155,7 +161,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
         hdr->abort_flag = 0;
         fence_mbarrier_init();
     }
-    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x)
         reinterpret_cast<uint32_t *>(one_s)[i] = 0x3F803F80u;  // bf16 1.0 pairs
     fence_proxy_async_smem();
     if (warp == 1) {
@@ -188,10 +194,19 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                 for (int c = 0; c < UCH; ++c)
                     tma_load_2d(u_s + (j * UCH + c) * R * 128, &tm_u, &hdr->u_full, nb * C::NB + j * SNB + c * 64, 0);
         }
+        // bias of each sub-block as an extra MMA K step: rows = filter columns, K = (hi, lo, 0, ...)
         for (int n = threadIdx.x; n < C::NB; n += blockDim.x) {
             const int gn = nb * C::NB + n;
-            b_s[n] = gn < p.N ? p.bias[gn] : 0.f;
+            const float bv = gn < p.N ? p.bias[gn] : 0.f;
+            const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv)));
+            const uint32_t lo =
+                static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv - __uint_as_float(hi << 16))));
+            const int j = n / SNB, r = n - j * SNB;
+            uint8_t *cm = bt_s + j * (SNB * 32) + ((r >> 3) * 2) * 128 + (r & 7) * 16;
+            *reinterpret_cast<uint4 *>(cm) = make_uint4(hi | (lo << 16), 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(cm + 128) = make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();
         __syncthreads();
 
         if (warp == 0) {
@@ -223,6 +238,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
         } else if (warp == 1) {
             // ---------------- MMA issuer
             constexpr uint32_t ID_RC = idesc_bf16_f32(kM, SNB, false, true);
+            constexpr uint32_t ID_BIAS = idesc_bf16_f32(kM, SNB, false, false);
             const uint32_t ID_DZ = idesc_bf16_f32(kM, R, false, false);
             const uint32_t ID_DU = idesc_bf16_f32(kM, R, true, true);
             constexpr uint32_t ID_DB = idesc_bf16_f32(kM, 16, true, false);
@@ -277,6 +293,8 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                             umma_bf16(tmem + kColW, sdesc(zs + ks * 32, 16, 1024, 2),
                                       sdesc(us + j * UCH * R * 128 + ks * 2048, R * 128, 1024, 2), ID_RC,
                                       ks > 0 ? 1u : 0u);
+                        umma_bf16(tmem + kColW, sdesc(ones, 128, 256, 0),  // + 1 . bias (exact hi + lo)
+                                  sdesc(smem_u32(bt_s) + j * (SNB * 32), 128, 256, 0), ID_BIAS, 1u);
                         umma_commit(&hdr->accw_full);
                     }
                     __syncwarp();
@@ -329,60 +347,65 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                     }
                     tc_fence_after();
                     const int nv = (t0 + row < p.BT) ? cursor.taps(t0 + row, p.T, W, p.cu, p.n_docs) : W;
+                    const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
+                    const bool owned = row < MS;
                     uint32_t ghi[GPH][4 * W], glo[GPH][4 * W];
 #pragma unroll
                     for (int gi = 0; gi < GPH; ++gi) {
                         const int gl = h * GPH + gi;          // group within the sub-block
                         const int ch0 = j * SCB + gl * 8;     // first channel within the block
-                        uint32_t acc[8 * W];
+                        uint32_t acc[8 * W];                  // filter (bias included), column c*W + k
                         tmem_ld_cols<8 * W>(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColW + gl * 8 * W, acc);
-                        float gy[8];
+                        const uint4 gr = *reinterpret_cast<const uint4 *>(gys + swz_b<RB>(row, ch0 >> 3));
+                        uint4 xr[W];
+#pragma unroll
+                        for (int k = 0; k < W; ++k)
+                            xr[k] = *reinterpret_cast<const uint4 *>(xs + swz_b<RB>(row + (W - 1) - k, ch0 >> 3));
+                        float gy[8], go[8];
                         {
-                            const uint4 r4 = *reinterpret_cast<const uint4 *>(gys + swz_b<RB>(row, ch0 >> 3));
-                            const uint32_t wv[4] = {r4.x, r4.y, r4.z, r4.w};
+                            const uint32_t wv[4] = {gr.x, gr.y, gr.z, gr.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 gy[2 * e] = __uint_as_float(wv[e] << 16);
                                 gy[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
                             }
                         }
-                        float xk[W][8];
 #pragma unroll
-                        for (int k = 0; k < W; ++k) {
-                            const uint4 r4 = *reinterpret_cast<const uint4 *>(xs + swz_b<RB>(row + (W - 1) - k, ch0 >> 3));
-                            const uint32_t wv[4] = {r4.x, r4.y, r4.z, r4.w};
-                            const bool on = k < nv;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                xk[k][2 * e] = on ? __uint_as_float(wv[e] << 16) : 0.f;
-                                xk[k][2 * e + 1] = on ? __uint_as_float(wv[e] & 0xffff0000u) : 0.f;
-                            }
-                        }
+                        for (int c = 0; c < 8; ++c) go[c] = owned ? gy[c] : 0.f;  // G of a non-owned row is 0
                         tmem_ld_wait();
-                        const float *bb = b_s + ch0 * W;
-                        // dx: own tap-0 term plus the residual; the tap-k terms of this token go to token row-k
+                        // dx: residual + own tap-0 term; the tap-k terms (k >= 1) of this token go to token row-k
                         float dxv[8];
                         float pk[W > 1 ? W - 1 : 1][8];
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
-                            const float w0 = __uint_as_float(acc[c * W]) + bb[c * W];
-                            dxv[c] = fmaf(w0, gy[c], gy[c]);
+                            dxv[c] = fmaf(__uint_as_float(acc[c * W]), gy[c], gy[c]);
 #pragma unroll
-                            for (int k = 1; k < W; ++k) {
-                                const float wk = __uint_as_float(acc[c * W + k]) + bb[c * W + k];
-                                pk[k - 1][c] = k < nv ? wk * gy[c] : 0.f;
-                            }
+                            for (int k = 1; k < W; ++k) pk[k - 1][c] = __uint_as_float(acc[c * W + k]) * gy[c];
                         }
-                        // G = dy * x~ (owned rows only), split exactly into bf16 hi + lo, column order c*W + k
-                        const bool owned = row < MS;
+                        if (!full_taps) {
+#pragma unroll
+                            for (int k = 1; k < W; ++k)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) pk[k - 1][c] = k < nv ? pk[k - 1][c] : 0.f;
+                        }
+                        // G = dy * x~ in column order c*W + k, split exactly: hi = top 16 bits of the fp32 product,
+                        // lo = the rest (it has at most 8 significant bits, so its top 16 bits hold it exactly)
 #pragma unroll
                         for (int f = 0; f < 8 * W; f += 2) {
-                            float g0 = owned ? gy[f / W] * xk[f % W][f / W] : 0.f;
-                            float g1 = owned ? gy[(f + 1) / W] * xk[(f + 1) % W][(f + 1) / W] : 0.f;
-                            const uint32_t h0 = bf16_bits(g0), h1 = bf16_bits(g1);
-                            const float r0 = g0 - __uint_as_float(h0 << 16), r1 = g1 - __uint_as_float(h1 << 16);
-                            ghi[gi][f / 2] = h0 | (h1 << 16);
-                            glo[gi][f / 2] = bf16_bits(r0) | (bf16_bits(r1) << 16);
+                            const int c0 = f / W, k0 = f % W, c1 = (f + 1) / W, k1 = (f + 1) % W;
+                            const uint32_t xw0 = (&xr[k0].x)[c0 >> 1], xw1 = (&xr[k1].x)[c1 >> 1];
+                            float x0 = __uint_as_float((c0 & 1) ? (xw0 & 0xffff0000u) : (xw0 << 16));
+                            float x1 = __uint_as_float((c1 & 1) ? (xw1 & 0xffff0000u) : (xw1 << 16));
+                            if (!full_taps) {
+                                x0 = k0 < nv ? x0 : 0.f;
+                                x1 = k1 < nv ? x1 : 0.f;
+                            }
+                            const float g0 = go[c0] * x0, g1 = go[c1] * x1;
+                            const uint32_t b0 = __float_as_uint(g0), b1 = __float_as_uint(g1);
+                            const float l0 = g0 - __uint_as_float(b0 & 0xffff0000u);
+                            const float l1 = g1 - __uint_as_float(b1 & 0xffff0000u);
+                            ghi[gi][f / 2] = __byte_perm(b0, b1, 0x7632);
+                            glo[gi][f / 2] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
                         }
                         if constexpr (W > 1) {
                             // rows row+k of this warp by shuffle; the first W-1 rows of the next quadrant by edge buffer
@@ -479,11 +502,11 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                         tmem_ld_x8(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColDz + (ip & 1) * R + c0, a8);
                         tmem_ld_wait();
                         if (row < MS && tp < p.BT) {
-                            float4 *dst = reinterpret_cast<float4 *>(p.dz_ws + static_cast<size_t>(tp) * R + c0);
-                            atomicAdd(dst, make_float4(__uint_as_float(a8[0]), __uint_as_float(a8[1]),
-                                                       __uint_as_float(a8[2]), __uint_as_float(a8[3])));
-                            atomicAdd(dst + 1, make_float4(__uint_as_float(a8[4]), __uint_as_float(a8[5]),
-                                                           __uint_as_float(a8[6]), __uint_as_float(a8[7])));
+                            float *dst = p.dz_ws + static_cast<size_t>(tp) * R + c0;
+                            red_add_v4(dst, __uint_as_float(a8[0]), __uint_as_float(a8[1]), __uint_as_float(a8[2]),
+                                       __uint_as_float(a8[3]));
+                            red_add_v4(dst + 4, __uint_as_float(a8[4]), __uint_as_float(a8[5]), __uint_as_float(a8[6]),
+                                       __uint_as_float(a8[7]));
                         }
                     }
                     tc_fence_before();
@@ -502,11 +525,11 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                     tmem_ld_x8(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColDz + (ip & 1) * R + c0, a8);
                     tmem_ld_wait();
                     if (row < MS && tp < p.BT && !*abort_flag) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.dz_ws + static_cast<size_t>(tp) * R + c0);
-                        atomicAdd(dst, make_float4(__uint_as_float(a8[0]), __uint_as_float(a8[1]),
-                                                   __uint_as_float(a8[2]), __uint_as_float(a8[3])));
-                        atomicAdd(dst + 1, make_float4(__uint_as_float(a8[4]), __uint_as_float(a8[5]),
-                                                       __uint_as_float(a8[6]), __uint_as_float(a8[7])));
+                        float *dst = p.dz_ws + static_cast<size_t>(tp) * R + c0;
+                        red_add_v4(dst, __uint_as_float(a8[0]), __uint_as_float(a8[1]), __uint_as_float(a8[2]),
+                                   __uint_as_float(a8[3]));
+                        red_add_v4(dst + 4, __uint_as_float(a8[4]), __uint_as_float(a8[5]), __uint_as_float(a8[6]),
+                                   __uint_as_float(a8[7]));
                     }
                 }
                 __syncwarp();
@@ -615,10 +638,10 @@ static dsc_status launch_lowrank_bwd(const LowrankArgs &a, const DeviceInfo &dev
     p.u_off = off;
     p.u_bytes = C::NSB * C::UCH * R * 128;
     off += p.u_bytes;
-    p.b_off = align_up(off, 128);
-    off = p.b_off + C::NB * 4;
+    p.bt_off = align_up(off, 1024);
+    off = p.bt_off + C::NSB * C::SNB * 32;
     p.one_off = align_up(off, 1024);
-    off = p.one_off + 1024;
+    off = p.one_off + 4096;
     p.g_off = align_up(off, 1024);
     off = p.g_off + 2 * 32768;
     p.dx_off = align_up(off, 1024);
