@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
     uint8_t *base = smem_raw + 1024;
     base += (1024u - (smem_u32(base) & 1023u)) & 1023u;
     uint8_t *u_s = base + p.u_off;                            // [NSB][UCH][R rows][128 B]
-    uint8_t *bt_s = base + p.bt_off;                          // bias as MMA B tiles: [NSB][SNB rows][16 K], no swizzle
+    uint8_t *bt_s = base + p.bt_off;                          // bias as MMA B tiles (K half 0 per sub-block, shared zero K half 1)
     uint8_t *one_s = base + p.one_off;                        // 4 KB of bf16 ones (an MMA A tile of 128 x 16)
     uint8_t *g_s = base + p.g_off;                            // [2 (hi, lo)][2 chunks][128 rows][128 B]
     uint8_t *dx_s = base + p.dx_off;                          // [128 rows][RB], swizzled
@@ -202,10 +202,13 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
             const uint32_t lo =
                 static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv - __uint_as_float(hi << 16))));
             const int j = n / SNB, r = n - j * SNB;
-            uint8_t *cm = bt_s + j * (SNB * 32) + ((r >> 3) * 2) * 128 + (r & 7) * 16;
-            *reinterpret_cast<uint4 *>(cm) = make_uint4(hi | (lo << 16), 0u, 0u, 0u);
-            *reinterpret_cast<uint4 *>(cm + 128) = make_uint4(0u, 0u, 0u, 0u);
+            // core matrices of 8 rows x 16 B: K half 0 of sub-block j at j*SNB*16 + (r/8)*128; every K half 1
+            // is the zero region that follows the NSB sub-blocks
+            *reinterpret_cast<uint4 *>(bt_s + j * (SNB * 16) + (r >> 3) * 128 + (r & 7) * 16) =
+                make_uint4(hi | (lo << 16), 0u, 0u, 0u);
         }
+        for (int i = threadIdx.x; i < SNB * 16 / 16; i += blockDim.x)
+            reinterpret_cast<uint4 *>(bt_s + NSB * SNB * 16)[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
         __syncthreads();
 
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                                       sdesc(us + j * UCH * R * 128 + ks * 2048, R * 128, 1024, 2), ID_RC,
                                       ks > 0 ? 1u : 0u);
                         umma_bf16(tmem + kColW, sdesc(ones, 128, 256, 0),  // + 1 . bias (exact hi + lo)
-                                  sdesc(smem_u32(bt_s) + j * (SNB * 32), 128, 256, 0), ID_BIAS, 1u);
+                                  sdesc(smem_u32(bt_s) + j * (SNB * 16), (NSB - j) * (SNB * 16), 128, 0), ID_BIAS, 1u);
                         umma_commit(&hdr->accw_full);
                     }
                     __syncwarp();
@@ -639,7 +642,7 @@ static dsc_status launch_lowrank_bwd(const LowrankArgs &a, const DeviceInfo &dev
     p.u_bytes = C::NSB * C::UCH * R * 128;
     off += p.u_bytes;
     p.bt_off = align_up(off, 1024);
-    off = p.bt_off + C::NSB * C::SNB * 32;
+    off = p.bt_off + (C::NSB + 1) * C::SNB * 16;
     p.one_off = align_up(off, 1024);
     off = p.one_off + 4096;
     p.g_off = align_up(off, 1024);
@@ -654,8 +657,8 @@ static dsc_status launch_lowrank_bwd(const LowrankArgs &a, const DeviceInfo &dev
     p.x_bytes = C::XR * C::RB;
     p.dy_in = align_up(p.x_in + p.x_bytes, 1024);
     p.dy_bytes = kM * C::RB;
-    p.nv_in = align_up(p.dy_in + p.dy_bytes, 128);
-    p.stage_bytes = align_up(p.nv_in + kM, 1024);
+    p.nv_in = 0;
+    p.stage_bytes = align_up(p.dy_in + p.dy_bytes, 1024);
     const unsigned smem = 2048 + p.st_off + kStages * p.stage_bytes;
     if (smem > static_cast<unsigned>(dev.max_smem_optin)) return DSC_ERR_UNSUPPORTED;
     p.status = device_status_word();
