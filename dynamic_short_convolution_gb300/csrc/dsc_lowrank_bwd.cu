@@ -12,17 +12,22 @@
 // its first MS tokens, and the last W-1 rows only feed the dx of owned tokens
 // (their filter rows come out of the same M=128 MMA).  A persistent CTA walks a
 // block-major run of units; per block it keeps U's columns resident (TMA, 128-B
-// swizzle) and accumulates dU^T and db in TMEM over all of its tiles.
-// The block is processed in NSB sub-blocks of SNB <= 128 columns:
-//   MMA  Wt_sub = z . U_sub                (A z K-major; B U_sub MN-major)   -> TMEM acc_W
+// swizzle) and accumulates dU and db in TMEM over all of its tiles.
+// Each tile is processed in NSB steps of SNB <= 128 filter columns, so that every
+// MMA but dz has N >= 96 (a tcgen05 MMA of N <= 64 costs about as much as N = 128):
+//   MMA  Wt_sub  = z . U_sub + 1 . b_sub       (A z K-major; B U_sub MN-major)  -> TMEM
 //   epi  dx, and G = dy * x~ split exactly into bf16 hi + lo (a product of two
-//        bf16 values has 16 significant bits), written K-major to smem
-//   MMA  dz  += G . U_sub^T               (A G K-major;  B U_sub K-major)   -> TMEM acc_dz
-//        dU^T += G^T . z                   (A G MN-major; B z MN-major)      -> TMEM acc_dU
-//        db   += G^T . 1                   (B an all-ones tile)              -> TMEM acc_db
+//        bf16 values has 16 significant bits), written K-major to shared memory
+//   MMA  dz     += G . U_sub^T                 (A G K-major; B U_sub K-major)   -> TMEM, per tile
+//        [dU; db] += [z^T; 1] . G               (A MN-major: z then an all-ones block; B G MN-major)
+//                                               -> TMEM rows 0..R-1 = dU, rows 64..127 = db
+// The filter accumulator is handed back as soon as the epilogue has loaded it, so
+// the next step's recompute overlaps the epilogue's arithmetic.  dx is written
+// over dy in the stage (each dy element is read only by the thread that overwrites
+// it) and stored by the producer warp once the tile is done.
 // dz partial sums of a tile over this block's columns are added with vector
-// atomics into an fp32 workspace (one partial per block); a last small kernel
-// rounds them to bf16.  dU and db are added atomically once per run of tiles.
+// reductions into an fp32 workspace (one partial per block); a last small
+// kernel rounds them to bf16.  dU and db are added once per run of tiles.
 // Row exchange for dx: the tap-k term of token t lands on token t-k, which is
 // another TMEM lane: warp shuffles inside a warp, a small shared edge buffer
 // across the four lane quadrants.
@@ -36,28 +41,41 @@ namespace dsc {
 namespace lrb {
 
 constexpr int kM = 128;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kStages = 2;
 constexpr int kTmemCols = 512;
-constexpr int kColW = 0;    // filter recompute accumulator, <= 128 columns
-constexpr int kColDz = 128; // two dz accumulators of R <= 64 columns
-constexpr int kColDu = 256; // NSB <= 2 dU^T accumulators of R columns
-constexpr int kColDb = 384; // NSB db accumulators of 16 columns
+constexpr int kColW = 0;        // filter accumulator, SNB <= 128 columns
+constexpr int kColDz = 128;     // two dz accumulators of R <= 64 columns
+constexpr int kColDu = 256;     // [dU; db] accumulator, NSB * SNB <= 256 columns
+constexpr int kGBlock = 16384;  // one 64-column block of G: 128 rows x 128 B
+constexpr int kGPart = 2 * kGBlock;
+
+// Channels per step: the largest multiple of 8 that divides CB with SCB*W <= 128
+// and SCB*W a multiple of 16 (the MMA N granularity).
+__host__ __device__ constexpr int step_channels(int W, int CB)
+{
+    for (int s = (128 / W) / 8 * 8; s >= 8; s -= 8)
+        if (s <= CB && CB % s == 0 && (s * W) % 16 == 0) return s;
+    return 0;
+}
 
 template <int W, int CB>
 struct Cfg {
     static constexpr int NB = CB * W;
-    static constexpr int SCB = (W <= 2) ? CB : (W <= 4 ? 32 : 16);  // channels per sub-block
+    static constexpr int SCB = step_channels(W, CB);
     static constexpr int NSB = CB / SCB;
-    static constexpr int SNB = SCB * W;                             // columns per sub-block
-    static constexpr int UCH = (SNB + 63) / 64;                     // 64-column chunks per U sub-tile
-    static constexpr int GPS = SCB / 8;                             // 8-channel groups per sub-block
-    static constexpr int GPH = GPS / 2;                             // groups per epilogue half
-    static constexpr int RB = CB * 2;                               // bytes per x / dy / dx row
+    static constexpr int SNB = SCB * W;                  // filter columns per step (MMA N)
+    static constexpr int GB = (SNB + 63) / 64;           // 64-column blocks of G and of a U step
+    static constexpr int GPS = SCB / 8;                  // 8-channel groups per step
+    static constexpr int NCA = GPS < 4 ? GPS : 4;        // column warps with work
+    static constexpr int GPW = GPS / NCA;                // groups per working warp
+    static constexpr int RB = CB * 2;                    // bytes per x / dy / dx row
     static constexpr int XR = kM + W - 1;
-    static constexpr int MS = kM - (W - 1);                         // owned tokens per tile
-    static_assert(SNB % 16 == 0 && SNB <= 128 && NSB <= 2 && GPH >= 1, "sub-block shape");
+    static constexpr int MS = kM - (W - 1);              // owned tokens per tile
+    static constexpr int QDU = NSB * SNB / 4;            // dU columns flushed per column warp
+    static_assert(SCB >= 8 && SNB <= 128 && SNB % 16 == 0 && NSB * SNB <= 256 && GPS % NCA == 0, "step shape");
+    static_assert(QDU % 8 == 0, "flush chunks");
 };
 
 struct Params {
@@ -69,8 +87,8 @@ struct Params {
     float *db;
     int BT, T, D, R, N;
     int n_nb, n_mt, n_units, MS;
-    unsigned u_off, bt_off, one_off, g_off, dx_off, e_off, st_off, stage_bytes;
-    unsigned u_bytes, z_bytes, x_in, x_bytes, dy_in, dy_bytes, nv_in;
+    unsigned u_off, bt_off, one_off, g_off, e_off, st_off, stage_bytes;
+    unsigned u_bytes, z_bytes, x_in, x_bytes, dy_in, dy_bytes;
     int *status;
     unsigned long long wait_ns;
 };
@@ -78,9 +96,10 @@ struct Params {
 struct Header {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t dx_full[kStages];
     uint64_t u_full;
     uint64_t accw_full, accw_empty;
-    uint64_t g_full[2], g_empty[2];
+    uint64_t g_full, g_empty;
     uint64_t dz_full[2], dz_empty[2];
     uint64_t flush;
     uint32_t tmem_base;
@@ -102,11 +121,6 @@ __device__ __forceinline__ uint32_t swz_b(int row, int c)
     else return row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float v)
-{
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
-}
-
 // Bounded wait that records a timeout and sets the CTA abort flag, but lets the
 // caller continue (used where a warp may not leave its group mid-step).
 __device__ __forceinline__ void wait_or_flag(uint64_t *bar, uint32_t parity, unsigned long long ns, int *status,
@@ -126,18 +140,16 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
 {
     using namespace lrb;
     using C = Cfg<W, CB>;
-    constexpr int NSB = C::NSB, SNB = C::SNB, UCH = C::UCH, GPH = C::GPH, RB = C::RB, SCB = C::SCB;
-    constexpr int MS = C::MS;
+    constexpr int NSB = C::NSB, SNB = C::SNB, GB = C::GB, GPW = C::GPW, RB = C::RB, SCB = C::SCB, MS = C::MS;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Header *hdr = reinterpret_cast<Header *>(smem_raw);
     uint8_t *base = smem_raw + 1024;
     base += (1024u - (smem_u32(base) & 1023u)) & 1023u;
-    uint8_t *u_s = base + p.u_off;                            // [NSB][UCH][R rows][128 B]
-    uint8_t *bt_s = base + p.bt_off;                          // bias as MMA B tiles (K half 0 per sub-block, shared zero K half 1)
-    uint8_t *one_s = base + p.one_off;                        // 4 KB of bf16 ones (an MMA A tile of 128 x 16)
-    uint8_t *g_s = base + p.g_off;                            // [2 (hi, lo)][2 chunks][128 rows][128 B]
-    uint8_t *dx_s = base + p.dx_off;                          // [128 rows][RB], swizzled
+    uint8_t *u_s = base + p.u_off;       // [NSB][GB][R rows][128 B]: U columns of each step, 128-B swizzle
+    uint8_t *bt_s = base + p.bt_off;     // bias as MMA B tiles (K half 0 per step, one shared zero K half 1)
+    uint8_t *one_s = base + p.one_off;   // 4 KB of bf16 ones, above every stage
+    uint8_t *g_s = base + p.g_off;       // [hi, lo][GB][128 rows][128 B]: G, swizzled
     float2 *edge = reinterpret_cast<float2 *>(base + p.e_off);
     uint8_t *stages = base + p.st_off;
 
@@ -146,14 +158,15 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&hdr->full[s], 1);
-            mbar_init(&hdr->empty[s], 1 + kEpiWarps);
+            mbar_init(&hdr->empty[s], 1);
+            mbar_init(&hdr->dx_full[s], kEpiWarps);
         }
         mbar_init(&hdr->u_full, 1);
         mbar_init(&hdr->accw_full, 1);
         mbar_init(&hdr->accw_empty, kEpiWarps);
+        mbar_init(&hdr->g_full, kEpiWarps);
+        mbar_init(&hdr->g_empty, 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&hdr->g_full[b], kEpiWarps);
-            mbar_init(&hdr->g_empty[b], 1);
             mbar_init(&hdr->dz_full[b], 1);
             mbar_init(&hdr->dz_empty[b], kEpiWarps);
         }
@@ -187,129 +200,164 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
         const int seg_end = min(u_end, (nb + 1) * p.n_mt);
         const int ntiles = seg_end - u;
 
-        // ---- U columns of this block (TMA) and its bias
+        // ---- U columns of this block (TMA, 64-column boxes per step) and its bias
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(&hdr->u_full, p.u_bytes);
             for (int j = 0; j < NSB; ++j)
-                for (int c = 0; c < UCH; ++c)
-                    tma_load_2d(u_s + (j * UCH + c) * R * 128, &tm_u, &hdr->u_full, nb * C::NB + j * SNB + c * 64, 0);
+                for (int b = 0; b < GB; ++b)
+                    tma_load_2d(u_s + (j * GB + b) * R * 128, &tm_u, &hdr->u_full, nb * C::NB + j * SNB + b * 64, 0);
         }
-        // bias of each sub-block as an extra MMA K step: rows = filter columns, K = (hi, lo, 0, ...)
-        for (int n = threadIdx.x; n < C::NB; n += blockDim.x) {
+        // bias of each step as an extra MMA K step: rows = filter columns, K = (hi, lo, 0, ...)
+        for (int n = threadIdx.x; n < NSB * SNB; n += blockDim.x) {
+            const int j = n / SNB, r = n - j * SNB;
             const int gn = nb * C::NB + n;
             const float bv = gn < p.N ? p.bias[gn] : 0.f;
             const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv)));
             const uint32_t lo =
                 static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv - __uint_as_float(hi << 16))));
-            const int j = n / SNB, r = n - j * SNB;
-            // core matrices of 8 rows x 16 B: K half 0 of sub-block j at j*SNB*16 + (r/8)*128; every K half 1
-            // is the zero region that follows the NSB sub-blocks
+            // core matrices of 8 rows x 16 B: K half 0 of step j at j*SNB*16 + (r/8)*128
             *reinterpret_cast<uint4 *>(bt_s + j * (SNB * 16) + (r >> 3) * 128 + (r & 7) * 16) =
                 make_uint4(hi | (lo << 16), 0u, 0u, 0u);
         }
-        for (int i = threadIdx.x; i < SNB * 16 / 16; i += blockDim.x)
+        for (int i = threadIdx.x; i < SNB; i += blockDim.x)  // the shared zero K half
             reinterpret_cast<uint4 *>(bt_s + NSB * SNB * 16)[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
         __syncthreads();
 
         if (warp == 0) {
-            // ---------------- producer: z, x (with the causal halo) and dy tiles
+            // ---------------- producer: z, x (with the causal halo) and dy tiles in; dx tiles out
+            bool ok = true;
             for (int v = 0; v < ntiles; ++v) {
                 const int i = it + v;
                 const int s = i % kStages;
-                const uint32_t ph = (i / kStages) & 1;
-                bool ok = mbar_wait(&hdr->empty[s], ph ^ 1, p.wait_ns);
-                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        record_status(p.status, kStatusTimeout);
-                        *abort_flag = 1;
-                    }
-                    break;
+                if (i >= kStages) {  // stage s last held tile i-2: its MMAs and its epilogue are done
+                    const uint32_t par = ((i / kStages) & 1) ^ 1;
+                    ok = mbar_wait(&hdr->empty[s], par, p.wait_ns);
+                    ok = mbar_wait(&hdr->dx_full[s], par, p.wait_ns) && ok;
                 }
+                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+                if (!ok) break;
                 const int mt = u + v - nb * p.n_mt;
-                const int t0 = mt * MS;
                 uint8_t *st = stages + s * p.stage_bytes;
                 if (lane == 0) {
+                    if (v >= kStages) {  // dx of tile i-2 (same run) sits over its dy
+                        tma_store_2d(&tm_dx, st + p.dy_in, nb * CB, (mt - kStages) * MS);
+                        tma_store_commit();
+                        tma_store_wait_read<0>();
+                    }
+                    const int t0 = mt * MS;
                     mbar_arrive_expect_tx(&hdr->full[s], p.z_bytes + p.x_bytes + p.dy_bytes);
                     tma_load_2d(st, &tm_z, &hdr->full[s], 0, t0);
                     tma_load_2d(st + p.x_in, &tm_x, &hdr->full[s], nb * CB, t0 - (W - 1));
                     tma_load_2d(st + p.dy_in, &tm_dy, &hdr->full[s], nb * CB, t0);
                     issued_last[s] = i;
                 }
-            }
-        } else if (warp == 1) {
-            // ---------------- MMA issuer
-            constexpr uint32_t ID_RC = idesc_bf16_f32(kM, SNB, false, true);
-            constexpr uint32_t ID_BIAS = idesc_bf16_f32(kM, SNB, false, false);
-            const uint32_t ID_DZ = idesc_bf16_f32(kM, R, false, false);
-            const uint32_t ID_DU = idesc_bf16_f32(kM, R, true, true);
-            constexpr uint32_t ID_DB = idesc_bf16_f32(kM, 16, true, false);
-            const uint32_t us = smem_u32(u_s), gs = smem_u32(g_s), ones = smem_u32(one_s);
-            bool ok = mbar_wait(&hdr->u_full, seg & 1, p.wait_ns);
-            int prev_i = -1, prev_j = 0, prev_s = 0;
-            auto issue_dzdu = [&](int i, int j, int s) {
-                const bool first_tile = (i == it);
-                const uint32_t zs = smem_u32(stages + s * p.stage_bytes);
-                const int step = i * NSB + j;
-                for (int part = 0; part < 2; ++part) {
-                    ok = mbar_wait(&hdr->g_full[part], step & 1, p.wait_ns) && ok;
-                    if (j == 0 && part == 0) ok = mbar_wait(&hdr->dz_empty[i & 1], ((i >> 1) & 1) ^ 1, p.wait_ns) && ok;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t gb = gs + part * 32768;
-                        for (int ks = 0; ks < SNB / 16; ++ks) {  // dz += G . U_sub^T over this sub-block's columns
-                            const int a = ks >> 2, kq = ks & 3;
-                            umma_bf16(tmem + kColDz + (i & 1) * R, sdesc(gb + a * 16384 + kq * 32, 16, 1024, 2),
-                                      sdesc(us + (j * UCH + a) * R * 128 + kq * 32, 16, 1024, 2), ID_DZ,
-                                      (j == 0 && part == 0 && ks == 0) ? 0u : 1u);
-                        }
-                        for (int ks = 0; ks < kM / 16; ++ks) {  // dU^T += G^T . z and db += G^T . 1 over the tokens
-                            const uint64_t ad = sdesc(gb + ks * 2048, 16384, 1024, 2);
-                            const uint32_t acc = (first_tile && part == 0 && ks == 0) ? 0u : 1u;
-                            umma_bf16(tmem + kColDu + j * R, ad, sdesc(zs + ks * 2048, 16384, 1024, 2), ID_DU, acc);
-                            umma_bf16(tmem + kColDb + j * 16, ad, sdesc(ones, 128, 256, 0), ID_DB, acc);
-                        }
-                        umma_commit(&hdr->g_empty[part]);
-                    }
-                    __syncwarp();
-                }
-                if (j == NSB - 1 && lane == 0) {
-                    umma_commit(&hdr->dz_full[i & 1]);
-                    umma_commit(&hdr->empty[s]);
-                }
                 __syncwarp();
-            };
-            for (int v = 0; v < ntiles && ok; ++v) {
+            }
+            // the dx of the run's last (up to two) tiles
+            for (int v = ntiles > kStages ? ntiles - kStages : 0; v < ntiles && ok; ++v) {
                 const int i = it + v;
                 const int s = i % kStages;
-                for (int j = 0; j < NSB; ++j) {
-                    const int step = i * NSB + j;
+                ok = mbar_wait(&hdr->dx_full[s], (i / kStages) & 1, p.wait_ns);
+                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+                if (ok && lane == 0) {
+                    tma_store_2d(&tm_dx, stages + s * p.stage_bytes + p.dy_in, nb * CB, (u + v - nb * p.n_mt) * MS);
+                    tma_store_commit();
+                }
+            }
+            if (lane == 0) tma_store_wait_read<0>();  // the stages may be refilled by the next run
+            if (!ok && lane == 0) {
+                record_status(p.status, kStatusTimeout);
+                *abort_flag = 1;
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            // ---------------- MMA issuer: per step k, the filter of step k and the gradients of step k-1
+            constexpr uint32_t ID_RC = idesc_bf16_f32(kM, SNB, false, true);
+            constexpr uint32_t ID_BIAS = idesc_bf16_f32(kM, SNB, false, false);
+            constexpr uint32_t ID_DU = idesc_bf16_f32(kM, SNB, true, true);
+            const uint32_t ID_DZ = idesc_bf16_f32(kM, R, false, false);
+            const uint32_t ones = smem_u32(one_s), st0 = smem_u32(stages);
+            // descriptors are built once; a K step, block or buffer change adds (byte offset >> 4) to the
+            // start-address field (bits 0-13), which never carries: shared addresses stay below 256 KB
+            const uint64_t d_g = sdesc(smem_u32(g_s), kGBlock, 1024, 2);  // G, MN-major (dU B): LBO = block stride
+            const uint64_t d_gk = sdesc(smem_u32(g_s), 16, 1024, 2);      // G, K-major (dz A)
+            const uint64_t d_u = sdesc(smem_u32(u_s), R * 128, 1024, 2);  // U step, MN-major (rc B): LBO = block stride
+            const uint64_t d_uk = sdesc(smem_u32(u_s), 16, 1024, 2);      // U step, K-major (dz B)
+            const uint64_t d_z = sdesc(st0, 16, 1024, 2);                 // z tile, K-major (rc A)
+            const uint64_t d_one = sdesc(ones, 128, 256, 0);              // all-ones A of the bias step
+            const uint64_t d_bt = sdesc(smem_u32(bt_s), 0, 128, 0);       // bias B; LBO set per step
+            const uint32_t ublk = static_cast<uint32_t>(R * 128) >> 4;     // one U block, descriptor units
+            const int nkr = R / 16;
+            bool ok = mbar_wait(&hdr->u_full, seg & 1, p.wait_ns);
+            const int k0 = it * NSB, nsteps = ntiles * NSB;
+            for (int kk = 0; kk <= nsteps && ok; ++kk) {
+                const int k = k0 + kk;
+                if (kk < nsteps) {
+                    // filter of step k: once the epilogue holds step k-1's filter in registers
+                    const int i = k / NSB, j = k - i * NSB, s = i % kStages;
                     if (j == 0) ok = mbar_wait(&hdr->full[s], (i / kStages) & 1, p.wait_ns) && ok;
-                    ok = mbar_wait(&hdr->accw_empty, (step & 1) ^ 1, p.wait_ns) && ok;
+                    ok = mbar_wait(&hdr->accw_empty, (k & 1) ^ 1, p.wait_ns) && ok;
                     ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
                     if (!ok) break;
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t zs = smem_u32(stages + s * p.stage_bytes);
-                        for (int ks = 0; ks < R / 16; ++ks)  // Wt_sub = z . U_sub (K = R)
-                            umma_bf16(tmem + kColW, sdesc(zs + ks * 32, 16, 1024, 2),
-                                      sdesc(us + j * UCH * R * 128 + ks * 2048, R * 128, 1024, 2), ID_RC,
-                                      ks > 0 ? 1u : 0u);
-                        umma_bf16(tmem + kColW, sdesc(ones, 128, 256, 0),  // + 1 . bias (exact hi + lo)
-                                  sdesc(smem_u32(bt_s) + j * (SNB * 16), (NSB - j) * (SNB * 16), 128, 0), ID_BIAS, 1u);
+                        const uint64_t a_z = d_z + ((s * p.stage_bytes) >> 4);
+                        const uint64_t b_u = d_u + static_cast<uint32_t>(j * GB) * ublk;
+                        const uint32_t d = tmem + kColW;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)  // Wt_sub = z . U_sub, K = R: 32 B in z, 16 rows in U
+                            if (ks < nkr) umma_bf16_nc(d, a_z + 2 * ks, b_u + 128 * ks, ID_RC, ks > 0 ? 1u : 0u);
+                        // + 1 . bias (exact hi + lo): K half 0 at this step's tile, K half 1 the shared zero tile
+                        umma_bf16_nc(d, d_one,
+                                     d_bt + static_cast<uint32_t>(j * SNB) +
+                                         (static_cast<uint64_t>((NSB - j) * SNB) << 16),
+                                     ID_BIAS, 1u);
                         umma_commit(&hdr->accw_full);
                     }
                     __syncwarp();
                     mma_any = true;
-                    if (prev_i >= 0) issue_dzdu(prev_i, prev_j, prev_s);
-                    prev_i = i;
-                    prev_j = j;
-                    prev_s = s;
+                }
+                if (kk > 0) {
+                    // gradients of step k-1, once its G is in shared memory
+                    const int kg = k - 1;
+                    const int i = kg / NSB, j = kg - i * NSB, s = i % kStages;
+                    ok = mbar_wait(&hdr->g_full, kg & 1, p.wait_ns) && ok;
+                    if (j == 0) ok = mbar_wait(&hdr->dz_empty[i & 1], ((i >> 1) & 1) ^ 1, p.wait_ns) && ok;
+                    ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t zs = st0 + s * p.stage_bytes;
+                        // [z^T; 1], MN-major: the second 64-row block (the ones) lies LBO bytes above the z tile
+                        const uint64_t a_zt = sdesc(zs, ones - zs, 1024, 2);
+                        const uint64_t b_uk = d_uk + static_cast<uint32_t>(j * GB) * ublk;
+                        const uint32_t t_dz = tmem + kColDz + (i & 1) * R, t_du = tmem + kColDu + j * SNB;
+                        const uint32_t acc_dz = j > 0 ? 1u : 0u, acc_du = i > it ? 1u : 0u;
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {  // G = hi + lo
+                            const uint64_t ga = d_g + part * (kGPart >> 4), gak = d_gk + part * (kGPart >> 4);
+#pragma unroll
+                            for (int ks = 0; ks < SNB / 16; ++ks)  // dz += G . U_sub^T: K over the step's columns
+                                umma_bf16_nc(t_dz, gak + (ks / 4) * (kGBlock >> 4) + (ks % 4) * 2,
+                                             b_uk + (ks / 4) * ublk + (ks % 4) * 2, ID_DZ,
+                                             (part == 0 && ks == 0) ? acc_dz : 1u);
+#pragma unroll
+                            for (int ks = 0; ks < kM / 16; ++ks)  // [dU; db] += [z^T; 1] . G: K over 16-token rows
+                                umma_bf16_nc(t_du,
+                                             a_zt + static_cast<uint64_t>(128 * ks) -
+                                                 (static_cast<uint64_t>(128 * ks) << 16),
+                                             ga + 128 * ks, ID_DU, (part == 0 && ks == 0) ? acc_du : 1u);
+                        }
+                        umma_commit(&hdr->g_empty);
+                        if (j == NSB - 1) {
+                            umma_commit(&hdr->dz_full[i & 1]);
+                            umma_commit(&hdr->empty[s]);
+                        }
+                    }
+                    __syncwarp();
                 }
             }
-            ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
-            if (ok && prev_i >= 0) issue_dzdu(prev_i, prev_j, prev_s);
             if (lane == 0) umma_commit(&hdr->flush);
             if (!ok && lane == 0) {
                 record_status(p.status, kStatusTimeout);
@@ -317,11 +365,13 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
             }
             __syncwarp();
         } else {
-            // ---------------- epilogue
-            const int q = warp & 3, h = (warp - 2) >> 2;
+            // ---------------- epilogue: 16 warps, lane quadrant q, column warp c
+            const int q = warp & 3, c = (warp - 2) >> 2;
             const int row = q * 32 + lane;
-            const bool store_thread = (threadIdx.x == 64);
-            int gcount = 0;  // groups processed (edge-buffer parity), equal across a half
+            const bool active = c < C::NCA;
+            const bool owned = row < MS;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            int gcount = 0;  // groups processed (edge-buffer parity), equal across one column warp's quadrants
             bool epi_abort = false;
             DocCursor cursor;  // this thread's token increases from tile to tile within a run
             for (int v = 0; v < ntiles && !epi_abort; ++v) {
@@ -329,188 +379,212 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                 const int s = i % kStages;
                 const int mt = u + v - nb * p.n_mt;
                 const int t0 = mt * MS;
-                const uint8_t *st = stages + s * p.stage_bytes;
+                uint8_t *st = stages + s * p.stage_bytes;
                 const uint8_t *xs = st + p.x_in;
-                const uint8_t *gys = st + p.dy_in;
+                uint8_t *dys = st + p.dy_in;
+                int nv = W;
+                bool full_taps = true;
                 for (int j = 0; j < NSB && !epi_abort; ++j) {
-                    const int step = i * NSB + j;
-                    bool ok = mbar_wait(&hdr->accw_full, step & 1, p.wait_ns);
-                    if (j == 0) {
-                        ok = mbar_wait(&hdr->full[s], (i / kStages) & 1, p.wait_ns) && ok;
-                        if (store_thread) tma_store_wait_read<0>();  // dx staging free again
-                    }
+                    const int k = i * NSB + j;
+                    bool ok = mbar_wait(&hdr->accw_full, k & 1, p.wait_ns);
+                    if (j == 0) ok = mbar_wait(&hdr->full[s], (i / kStages) & 1, p.wait_ns) && ok;
                     ok = ok && (*abort_flag == 0);
-                    if (named_bar_any(1, 32 * kEpiWarps, !ok)) {  // every epilogue warp leaves together
-                        if (lane == 0) {
-                            record_status(p.status, kStatusTimeout);
-                            *abort_flag = 1;
+                    // A warp leaves only together with the warps it meets at a named barrier: the four quadrants
+                    // of a column warp decide at their exchange barrier; a warp with no such barrier decides alone.
+                    // Every other wait is bounded, so the rest of the CTA follows through the abort flag.
+                    bool bad = !ok;
+                    if (!(active && W > 1)) {
+                        if (__any_sync(0xffffffffu, bad)) {
+                            if (lane == 0) {
+                                record_status(p.status, kStatusTimeout);
+                                *abort_flag = 1;
+                            }
+                            epi_abort = true;
+                            break;
                         }
-                        epi_abort = true;
-                        break;
+                        bad = false;
                     }
                     tc_fence_after();
-                    const int nv = (t0 + row < p.BT) ? cursor.taps(t0 + row, p.T, W, p.cu, p.n_docs) : W;
-                    const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
-                    const bool owned = row < MS;
-                    uint32_t ghi[GPH][4 * W], glo[GPH][4 * W];
+                    if (j == 0) {
+                        nv = (t0 + row < p.BT) ? cursor.taps(t0 + row, p.T, W, p.cu, p.n_docs) : W;
+                        full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
+                    }
+                    // this warp's filter columns (bias included) of the step: group gl, column c*W + k
+                    uint32_t acc[GPW][8 * W];
+                    if (active) {
 #pragma unroll
-                    for (int gi = 0; gi < GPH; ++gi) {
-                        const int gl = h * GPH + gi;          // group within the sub-block
-                        const int ch0 = j * SCB + gl * 8;     // first channel within the block
-                        uint32_t acc[8 * W];                  // filter (bias included), column c*W + k
-                        tmem_ld_cols<8 * W>(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColW + gl * 8 * W, acc);
-                        const uint4 gr = *reinterpret_cast<const uint4 *>(gys + swz_b<RB>(row, ch0 >> 3));
-                        uint4 xr[W];
+                        for (int gi = 0; gi < GPW; ++gi)
+                            tmem_ld_cols<8 * W>(lane_base + kColW + (c * GPW + gi) * 8 * W, acc[gi]);
+                    }
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&hdr->accw_empty);  // the next step's filter may be computed
+                    if (active) {
 #pragma unroll
-                        for (int k = 0; k < W; ++k)
-                            xr[k] = *reinterpret_cast<const uint4 *>(xs + swz_b<RB>(row + (W - 1) - k, ch0 >> 3));
-                        float gy[8], go[8];
-                        {
-                            const uint32_t wv[4] = {gr.x, gr.y, gr.z, gr.w};
+                        for (int gi = 0; gi < GPW; ++gi) {
+                            const int gl = c * GPW + gi;       // group within the step
+                            const int ch0 = j * SCB + gl * 8;  // first channel within the block
+                            const uint32_t dy_off = swz_b<RB>(row, ch0 >> 3);
+                            float gy[8];  // dy of this token
+                            float dxv[8];
+                            {
+                                const uint4 gr = *reinterpret_cast<const uint4 *>(dys + dy_off);
+                                const uint32_t wv[4] = {gr.x, gr.y, gr.z, gr.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                gy[2 * e] = __uint_as_float(wv[e] << 16);
-                                gy[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
-                            }
-                        }
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) go[c] = owned ? gy[c] : 0.f;  // G of a non-owned row is 0
-                        tmem_ld_wait();
-                        // dx: residual + own tap-0 term; the tap-k terms (k >= 1) of this token go to token row-k
-                        float dxv[8];
-                        float pk[W > 1 ? W - 1 : 1][8];
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            dxv[c] = fmaf(__uint_as_float(acc[c * W]), gy[c], gy[c]);
-#pragma unroll
-                            for (int k = 1; k < W; ++k) pk[k - 1][c] = __uint_as_float(acc[c * W + k]) * gy[c];
-                        }
-                        if (!full_taps) {
-#pragma unroll
-                            for (int k = 1; k < W; ++k)
-#pragma unroll
-                                for (int c = 0; c < 8; ++c) pk[k - 1][c] = k < nv ? pk[k - 1][c] : 0.f;
-                        }
-                        // G = dy * x~ in column order c*W + k, split exactly: hi = top 16 bits of the fp32 product,
-                        // lo = the rest (it has at most 8 significant bits, so its top 16 bits hold it exactly)
-#pragma unroll
-                        for (int f = 0; f < 8 * W; f += 2) {
-                            const int c0 = f / W, k0 = f % W, c1 = (f + 1) / W, k1 = (f + 1) % W;
-                            const uint32_t xw0 = (&xr[k0].x)[c0 >> 1], xw1 = (&xr[k1].x)[c1 >> 1];
-                            float x0 = __uint_as_float((c0 & 1) ? (xw0 & 0xffff0000u) : (xw0 << 16));
-                            float x1 = __uint_as_float((c1 & 1) ? (xw1 & 0xffff0000u) : (xw1 << 16));
-                            if (!full_taps) {
-                                x0 = k0 < nv ? x0 : 0.f;
-                                x1 = k1 < nv ? x1 : 0.f;
-                            }
-                            const float g0 = go[c0] * x0, g1 = go[c1] * x1;
-                            const uint32_t b0 = __float_as_uint(g0), b1 = __float_as_uint(g1);
-                            const float l0 = g0 - __uint_as_float(b0 & 0xffff0000u);
-                            const float l1 = g1 - __uint_as_float(b1 & 0xffff0000u);
-                            ghi[gi][f / 2] = __byte_perm(b0, b1, 0x7632);
-                            glo[gi][f / 2] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
-                        }
-                        if constexpr (W > 1) {
-                            // rows row+k of this warp by shuffle; the first W-1 rows of the next quadrant by edge buffer
-                            const int par = gcount & 1;
-                            float2 *eh = edge + ((h * 4) * 2) * (W - 1) * (W - 1) * 4;  // [q][par][j][k-1][4]
-                            if (lane < W - 1) {
-#pragma unroll
-                                for (int k = 1; k < W; ++k) {
-                                    float2 *dst = eh + (((q * 2 + par) * (W - 1) + lane) * (W - 1) + (k - 1)) * 4;
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) dst[e] = make_float2(pk[k - 1][2 * e], pk[k - 1][2 * e + 1]);
+                                for (int e = 0; e < 4; ++e) {
+                                    gy[2 * e] = __uint_as_float(wv[e] << 16);
+                                    gy[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
                                 }
                             }
-                            float recv[W - 1][8];
+                            // dx: residual + own tap-0 term
 #pragma unroll
-                            for (int k = 1; k < W; ++k)
+                            for (int e = 0; e < 8; e += 2) {
+                                const float2 d2 = __ffma2_rn(
+                                    make_float2(__uint_as_float(acc[gi][e * W]), __uint_as_float(acc[gi][(e + 1) * W])),
+                                    make_float2(gy[e], gy[e + 1]), make_float2(gy[e], gy[e + 1]));
+                                dxv[e] = d2.x;
+                                dxv[e + 1] = d2.y;
+                            }
+                            if constexpr (W > 1) {
+                                // the tap-k term of this token goes to token row-k: rows of this warp by shuffle, one
+                                // tap at a time; the first W-1 rows of the next quadrant through the edge buffer
+                                // [c][q][par][lane][k-1][4]
+                                const int par = gcount & 1;
+                                float2 *eh = edge + c * (4 * 2 * (W - 1) * (W - 1) * 4);
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) recv[k - 1][c] = __shfl_down_sync(0xffffffffu, pk[k - 1][c], k);
-                            named_bar(2 + h, 32 * kEpiWarps / 2);
-                            if (q < 3) {
+                                for (int kk = 1; kk < W; ++kk) {
+                                    float pk[8];
 #pragma unroll
-                                for (int k = 1; k < W; ++k) {
-                                    if (lane + k >= 32) {
-                                        const float2 *src =
-                                            eh + ((((q + 1) * 2 + par) * (W - 1) + (lane + k - 32)) * (W - 1) + (k - 1)) * 4;
+                                    for (int e = 0; e < 8; e += 2) {
+                                        const float2 p2 = __fmul2_rn(make_float2(__uint_as_float(acc[gi][e * W + kk]),
+                                                                                 __uint_as_float(acc[gi][(e + 1) * W + kk])),
+                                                                     make_float2(gy[e], gy[e + 1]));
+                                        pk[e] = p2.x;
+                                        pk[e + 1] = p2.y;
+                                    }
+                                    if (!full_taps) {
 #pragma unroll
-                                        for (int e = 0; e < 4; ++e) {
-                                            const float2 v2 = src[e];
-                                            recv[k - 1][2 * e] = v2.x;
-                                            recv[k - 1][2 * e + 1] = v2.y;
+                                        for (int e = 0; e < 8; ++e) pk[e] = kk < nv ? pk[e] : 0.f;
+                                    }
+                                    if (lane < W - 1) {
+                                        float2 *dst = eh + (((q * 2 + par) * (W - 1) + lane) * (W - 1) + (kk - 1)) * 4;
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e) dst[e] = make_float2(pk[2 * e], pk[2 * e + 1]);
+                                    }
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        const float v = __shfl_down_sync(0xffffffffu, pk[e], kk);
+                                        dxv[e] += lane + kk < 32 ? v : 0.f;
+                                    }
+                                }
+                                if (named_bar_any(2 + c, 128, bad)) {
+                                    if (lane == 0) {
+                                        record_status(p.status, kStatusTimeout);
+                                        *abort_flag = 1;
+                                    }
+                                    epi_abort = true;
+                                    break;
+                                }
+                                if (q < 3) {  // the last quadrant's last W-1 rows are not owned
+#pragma unroll
+                                    for (int kk = 1; kk < W; ++kk) {
+                                        if (lane + kk >= 32) {
+                                            const float2 *src =
+                                                eh + ((((q + 1) * 2 + par) * (W - 1) + (lane + kk - 32)) * (W - 1) +
+                                                      (kk - 1)) * 4;
+#pragma unroll
+                                            for (int e = 0; e < 4; ++e) {
+                                                const float2 ev = src[e];
+                                                dxv[2 * e] += ev.x;
+                                                dxv[2 * e + 1] += ev.y;
+                                            }
                                         }
                                     }
                                 }
                             }
-#pragma unroll
-                            for (int k = 1; k < W; ++k)
-#pragma unroll
-                                for (int c = 0; c < 8; ++c) dxv[c] += recv[k - 1][c];
-                        }
-                        ++gcount;
-                        if (owned) {
-                            uint4 o;
-                            o.x = pack_bf16x2(dxv[0], dxv[1]);
-                            o.y = pack_bf16x2(dxv[2], dxv[3]);
-                            o.z = pack_bf16x2(dxv[4], dxv[5]);
-                            o.w = pack_bf16x2(dxv[6], dxv[7]);
-                            *reinterpret_cast<uint4 *>(dx_s + swz_b<RB>(row, ch0 >> 3)) = o;
-                        }
-                    }
-                    // the filter accumulator is consumed: the next sub-block may be recomputed
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&hdr->accw_empty);
-                    // G hi, then G lo, into the two operand buffers (each freed by the MMAs of the previous step)
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        wait_or_flag(&hdr->g_empty[part], (step & 1) ^ 1, p.wait_ns, p.status, abort_flag);
-                        uint8_t *gb = g_s + part * 32768;
-#pragma unroll
-                        for (int gi = 0; gi < GPH; ++gi) {
-                            const int gl = h * GPH + gi;
+                            ++gcount;
+                            // G of this group into the step's buffer, once the previous step's MMAs have read it
+                            if (gi == 0)
+                                wait_or_flag(&hdr->g_empty, (k & 1) ^ 1, p.wait_ns, p.status, abort_flag);
 #pragma unroll
                             for (int m = 0; m < W; ++m) {  // 16-byte chunk m of the group's 8W columns
+                                // G = dy * x~, column c*W + k: hi = top 16 bits of the fp32 product (exact), lo =
+                                // the rest (at most 8 significant bits, so its top 16 bits hold it exactly)
+                                uint32_t hi4[4], lo4[4];
+#pragma unroll
+                                for (int f2 = 0; f2 < 4; ++f2) {
+                                    const int f = m * 8 + 2 * f2;
+                                    const int c0 = f / W, k0 = f % W, c1 = (f + 1) / W, k1 = (f + 1) % W;
+                                    const uint32_t xw0 = *reinterpret_cast<const uint32_t *>(
+                                        xs + swz_b<RB>(row + (W - 1) - k0, ch0 >> 3) + (c0 >> 1) * 4);
+                                    const uint32_t xw1 = *reinterpret_cast<const uint32_t *>(
+                                        xs + swz_b<RB>(row + (W - 1) - k1, ch0 >> 3) + (c1 >> 1) * 4);
+                                    float x0 = __uint_as_float((c0 & 1) ? (xw0 & 0xffff0000u) : (xw0 << 16));
+                                    float x1 = __uint_as_float((c1 & 1) ? (xw1 & 0xffff0000u) : (xw1 << 16));
+                                    if (!full_taps) {
+                                        x0 = k0 < nv ? x0 : 0.f;
+                                        x1 = k1 < nv ? x1 : 0.f;
+                                    }
+                                    // G of a non-owned row is 0
+                                    const float2 g = __fmul2_rn(make_float2(owned ? gy[c0] : 0.f, owned ? gy[c1] : 0.f),
+                                                                make_float2(x0, x1));
+                                    const uint32_t b0 = __float_as_uint(g.x), b1 = __float_as_uint(g.y);
+                                    // lo = g - hi, exact (fused: g + (-1) * hi)
+                                    const float2 l = __ffma2_rn(make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                                                            __uint_as_float(b1 & 0xffff0000u)),
+                                                                make_float2(-1.f, -1.f), g);
+                                    hi4[f2] = __byte_perm(b0, b1, 0x7632);
+                                    lo4[f2] = __byte_perm(__float_as_uint(l.x), __float_as_uint(l.y), 0x7632);
+                                }
                                 const int col = gl * 8 * W + m * 8;
-                                const uint32_t *src = part == 0 ? &ghi[gi][m * 4] : &glo[gi][m * 4];
-                                *reinterpret_cast<uint4 *>(gb + (col >> 6) * 16384 + row * 128 +
-                                                           ((((col & 63) >> 3) ^ (row & 7)) << 4)) =
-                                    make_uint4(src[0], src[1], src[2], src[3]);
+                                const uint32_t off = (col >> 6) * kGBlock + row * 128 +
+                                                     ((((col & 63) >> 3) ^ (row & 7)) << 4);
+                                *reinterpret_cast<uint4 *>(g_s + off) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
+                                *reinterpret_cast<uint4 *>(g_s + kGPart + off) =
+                                    make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+                            }
+                            // dx over this token's dy (read above by this thread only)
+                            if (owned) {
+                                uint4 o;
+                                o.x = pack_bf16x2(dxv[0], dxv[1]);
+                                o.y = pack_bf16x2(dxv[2], dxv[3]);
+                                o.z = pack_bf16x2(dxv[4], dxv[5]);
+                                o.w = pack_bf16x2(dxv[6], dxv[7]);
+                                *reinterpret_cast<uint4 *>(dys + dy_off) = o;
                             }
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&hdr->g_full[part]);
+                    }
+                    if (epi_abort) break;
+                    // a warp without G to write still keeps step with the G buffer before it signals the step
+                    if (!active) wait_or_flag(&hdr->g_empty, (k & 1) ^ 1, p.wait_ns, p.status, abort_flag);
+                    // G of step k is written; after the tile's last step its dx is complete too
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&hdr->g_full);
+                        if (j == NSB - 1) mbar_arrive(&hdr->dx_full[s]);
                     }
                 }
                 if (epi_abort) break;
-                // this tile's x / dy are no longer needed; its dx tile is complete
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&hdr->empty[s]);
-                fence_proxy_async_smem();
-                named_bar(1, 32 * kEpiWarps);
-                if (store_thread) {
-                    tma_store_2d(&tm_dx, dx_s, nb * CB, t0);
-                    tma_store_commit();
-                }
                 // dz partial sums of the previous tile (its MMAs have had a whole tile to finish)
                 if (v > 0) {
                     const int ip = i - 1;
                     wait_or_flag(&hdr->dz_full[ip & 1], (ip >> 1) & 1, p.wait_ns, p.status, abort_flag);
                     tc_fence_after();
                     const int tp = (mt - 1) * MS + row;
-                    for (int c0 = h * (R / 2); c0 < (h + 1) * (R / 2); c0 += 8) {
-                        uint32_t a8[8];
-                        tmem_ld_x8(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColDz + (ip & 1) * R + c0, a8);
-                        tmem_ld_wait();
-                        if (row < MS && tp < p.BT) {
-                            float *dst = p.dz_ws + static_cast<size_t>(tp) * R + c0;
-                            red_add_v4(dst, __uint_as_float(a8[0]), __uint_as_float(a8[1]), __uint_as_float(a8[2]),
-                                       __uint_as_float(a8[3]));
-                            red_add_v4(dst + 4, __uint_as_float(a8[4]), __uint_as_float(a8[5]), __uint_as_float(a8[6]),
-                                       __uint_as_float(a8[7]));
-                        }
+                    uint32_t a[16];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        if (cc < R / 16) tmem_ld_x4(lane_base + kColDz + (ip & 1) * R + c * (R / 4) + cc * 4, a + 4 * cc);
+                    tmem_ld_wait();
+                    if (row < MS && tp < p.BT) {
+                        float *dst = p.dz_ws + static_cast<size_t>(tp) * R + c * (R / 4);
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            if (cc < R / 16)
+                                red_add_v4(dst + 4 * cc, __uint_as_float(a[4 * cc]), __uint_as_float(a[4 * cc + 1]),
+                                           __uint_as_float(a[4 * cc + 2]), __uint_as_float(a[4 * cc + 3]));
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -523,40 +597,34 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                 tc_fence_after();
                 const int ip = it + ntiles - 1;
                 const int tp = (seg_end - 1 - nb * p.n_mt) * MS + row;
-                for (int c0 = h * (R / 2); c0 < (h + 1) * (R / 2); c0 += 8) {
+                uint32_t a[16];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    if (cc < R / 16) tmem_ld_x4(lane_base + kColDz + (ip & 1) * R + c * (R / 4) + cc * 4, a + 4 * cc);
+                tmem_ld_wait();
+                if (row < MS && tp < p.BT && !*abort_flag) {
+                    float *dst = p.dz_ws + static_cast<size_t>(tp) * R + c * (R / 4);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        if (cc < R / 16)
+                            red_add_v4(dst + 4 * cc, __uint_as_float(a[4 * cc]), __uint_as_float(a[4 * cc + 1]),
+                                       __uint_as_float(a[4 * cc + 2]), __uint_as_float(a[4 * cc + 3]));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hdr->dz_empty[ip & 1]);
+                // [dU; db] accumulator: TMEM lane m < R is row m of dU, lane 64 is db; column j*SNB + n
+                const bool du_row = row < R, db_row = row == 64;
+                for (int cc = c * C::QDU; cc < (c + 1) * C::QDU; cc += 8) {
                     uint32_t a8[8];
-                    tmem_ld_x8(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColDz + (ip & 1) * R + c0, a8);
+                    tmem_ld_x8(lane_base + kColDu + cc, a8);
                     tmem_ld_wait();
-                    if (row < MS && tp < p.BT && !*abort_flag) {
-                        float *dst = p.dz_ws + static_cast<size_t>(tp) * R + c0;
+                    const int gn0 = nb * C::NB + cc;  // a multiple of 8; N is too, so all 8 are valid or none
+                    if ((du_row || db_row) && gn0 < p.N && !*abort_flag) {
+                        float *dst = du_row ? p.dU + static_cast<size_t>(row) * p.N + gn0 : p.db + gn0;
                         red_add_v4(dst, __uint_as_float(a8[0]), __uint_as_float(a8[1]), __uint_as_float(a8[2]),
                                    __uint_as_float(a8[3]));
                         red_add_v4(dst + 4, __uint_as_float(a8[4]), __uint_as_float(a8[5]), __uint_as_float(a8[6]),
                                    __uint_as_float(a8[7]));
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&hdr->dz_empty[ip & 1]);
-#pragma unroll
-                for (int j = 0; j < NSB; ++j) {
-                    const int n_local = row;  // dU^T / db lane = filter column within the sub-block
-                    const int gn = nb * C::NB + j * SNB + n_local;
-                    const bool valid = n_local < SNB && gn < p.N && !*abort_flag;
-                    for (int c0 = h * (R / 2); c0 < (h + 1) * (R / 2); c0 += 8) {
-                        uint32_t a8[8];
-                        tmem_ld_x8(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColDu + j * R + c0, a8);
-                        tmem_ld_wait();
-                        if (valid) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                atomicAdd(p.dU + static_cast<size_t>(c0 + e) * p.N + gn, __uint_as_float(a8[e]));
-                        }
-                    }
-                    if (h == 0) {
-                        uint32_t a8[8];
-                        tmem_ld_x8(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColDb + j * 16, a8);
-                        tmem_ld_wait();
-                        if (valid) atomicAdd(p.db + gn, __uint_as_float(a8[0]));
                     }
                 }
                 tc_fence_before();
@@ -570,12 +638,13 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
     }
 
     // ---- teardown: nothing of this CTA may still be in flight
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        for (int s = 0; s < kStages; ++s)
-            if (issued_last[s] >= 0) (void)mbar_wait(&hdr->full[s], (issued_last[s] / kStages) & 1, kDrainLimitNs);
+    if (warp == 0 && lane == 0) {
+        if (*abort_flag)
+            for (int s = 0; s < kStages; ++s)
+                if (issued_last[s] >= 0) (void)mbar_wait(&hdr->full[s], (issued_last[s] / kStages) & 1, kDrainLimitNs);
+        tma_store_wait_all<0>();
     }
     if (warp == 1 && lane == 0 && mma_any && *abort_flag) (void)mbar_wait(&hdr->flush, (seg - 1) & 1, kDrainLimitNs);
-    if (threadIdx.x == 64) tma_store_wait_all<0>();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -637,29 +706,28 @@ static dsc_status launch_lowrank_bwd(const LowrankArgs &a, const DeviceInfo &dev
     if (units > 0x7fffffffLL) return DSC_ERR_UNSUPPORTED;
     p.n_units = static_cast<int>(units);
     const int R = a.R;
+    // shared memory: [header][slack][U steps][bias tiles][G hi, lo][edges][stages x2][ones]
     unsigned off = 0;
     p.u_off = off;
-    p.u_bytes = C::NSB * C::UCH * R * 128;
+    p.u_bytes = C::NSB * C::GB * R * 128;
     off += p.u_bytes;
     p.bt_off = align_up(off, 1024);
     off = p.bt_off + (C::NSB + 1) * C::SNB * 16;
-    p.one_off = align_up(off, 1024);
-    off = p.one_off + 4096;
     p.g_off = align_up(off, 1024);
-    off = p.g_off + 2 * 32768;
-    p.dx_off = align_up(off, 1024);
-    off = p.dx_off + kM * C::RB;
+    off = p.g_off + 2 * kGPart;
     p.e_off = align_up(off, 128);
-    off = p.e_off + 2 * 4 * 2 * (W - 1) * (W - 1) * 32;
+    off = p.e_off + C::NCA * 4 * 2 * (W - 1) * (W - 1) * 32;
     p.st_off = align_up(off, 1024);
     p.z_bytes = 16384;
     p.x_in = p.z_bytes;
     p.x_bytes = C::XR * C::RB;
     p.dy_in = align_up(p.x_in + p.x_bytes, 1024);
     p.dy_bytes = kM * C::RB;
-    p.nv_in = 0;
     p.stage_bytes = align_up(p.dy_in + p.dy_bytes, 1024);
-    const unsigned smem = 2048 + p.st_off + kStages * p.stage_bytes;
+    // the all-ones block sits above every z tile: the dU MMA reaches it from a z tile through a positive
+    // leading-byte offset
+    p.one_off = p.st_off + kStages * p.stage_bytes;
+    const unsigned smem = 2048 + p.one_off + 4096;
     if (smem > static_cast<unsigned>(dev.max_smem_optin)) return DSC_ERR_UNSUPPORTED;
     p.status = device_status_word();
     p.wait_ns = wait_limit_ns();

@@ -94,6 +94,19 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// The same MMA without a compiler memory clobber, for long issue sequences whose
+// operands sit in registers: volatile asm statements keep their relative order, so
+// the MMA still follows the mbarrier waits and precedes the commit that tracks it.
+__device__ __forceinline__ void umma_bf16_nc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
 // Arrive once on `bar` when every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
@@ -105,6 +118,13 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
 
 // 32 TMEM lanes x N consecutive 32-bit columns: thread i of the warp receives
 // lane (lane base + i), columns col .. col+N-1.  Completes at tmem_ld_wait().
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t *r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t *r)
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
