@@ -504,6 +504,14 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                                 }
                             }
                             ++gcount;
+                            // x~ rows row+W-1-k of this group's 8 channels: one 16-byte load per tap (conflict-free
+                            // under the 128-byte swizzle) where registers allow, 4-byte loads otherwise
+                            uint4 xr[W <= 4 ? W : 1];
+                            if constexpr (W <= 4) {
+#pragma unroll
+                                for (int kk = 0; kk < W; ++kk)
+                                    xr[kk] = *reinterpret_cast<const uint4 *>(xs + swz_b<RB>(row + (W - 1) - kk, ch0 >> 3));
+                            }
                             // G of this group into the step's buffer, once the previous step's MMAs have read it
                             if (gi == 0)
                                 wait_or_flag(&hdr->g_empty, (k & 1) ^ 1, p.wait_ns, p.status, abort_flag);
@@ -516,10 +524,16 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                                 for (int f2 = 0; f2 < 4; ++f2) {
                                     const int f = m * 8 + 2 * f2;
                                     const int c0 = f / W, k0 = f % W, c1 = (f + 1) / W, k1 = (f + 1) % W;
-                                    const uint32_t xw0 = *reinterpret_cast<const uint32_t *>(
-                                        xs + swz_b<RB>(row + (W - 1) - k0, ch0 >> 3) + (c0 >> 1) * 4);
-                                    const uint32_t xw1 = *reinterpret_cast<const uint32_t *>(
-                                        xs + swz_b<RB>(row + (W - 1) - k1, ch0 >> 3) + (c1 >> 1) * 4);
+                                    uint32_t xw0, xw1;
+                                    if constexpr (W <= 4) {
+                                        xw0 = (&xr[k0].x)[c0 >> 1];
+                                        xw1 = (&xr[k1].x)[c1 >> 1];
+                                    } else {
+                                        xw0 = *reinterpret_cast<const uint32_t *>(
+                                            xs + swz_b<RB>(row + (W - 1) - k0, ch0 >> 3) + (c0 >> 1) * 4);
+                                        xw1 = *reinterpret_cast<const uint32_t *>(
+                                            xs + swz_b<RB>(row + (W - 1) - k1, ch0 >> 3) + (c1 >> 1) * 4);
+                                    }
                                     float x0 = __uint_as_float((c0 & 1) ? (xw0 & 0xffff0000u) : (xw0 << 16));
                                     float x1 = __uint_as_float((c1 & 1) ? (xw1 & 0xffff0000u) : (xw1 << 16));
                                     if (!full_taps) {
