@@ -73,6 +73,12 @@ def kernel_source_digest(files):
 
 DENSE_BWD_SRC = ["dsc_dense_bwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 DENSE_FWD_SRC = ["dsc_dense_fwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
+LOWRANK_BWD_SRC = ["dsc_lowrank_bwd.cu", "dsc_tcgen05.cuh", "dsc_device.cuh"]
+LOWRANK_FWD_SRC = ["dsc_lowrank_fwd.cu", "dsc_tcgen05.cuh", "dsc_device.cuh"]
+# (kernel name in the ncu launch list, source files) per workload kind and direction
+KERNELS = {("dense", "bwd"): ("dense_bwd_tma", DENSE_BWD_SRC), ("dense", "fwd"): ("dense_fwd_tma", DENSE_FWD_SRC),
+           ("lowrank", "bwd"): ("lowrank_bwd_tc", LOWRANK_BWD_SRC),
+           ("lowrank", "fwd"): ("lowrank_fwd_tc", LOWRANK_FWD_SRC)}
 
 
 def measured_traffic(kernel, workload, digest):
@@ -458,16 +464,23 @@ def main():
     step_bytes = prob.bytes_fwd + prob.bytes_bwd
     step_gbs = step_bytes / (total_ms / args.steps / 1e3) / 1e9
 
-    # roofline of the dominant kernel
-    if mean_b >= mean_f:
-        kname, kbytes, kms, ksrc = "dense_bwd_tma", prob.bytes_bwd, mean_b, DENSE_BWD_SRC
-    else:
-        kname, kbytes, kms, ksrc = "dense_fwd_tma", prob.bytes_fwd, mean_f, DENSE_FWD_SRC
-    achieved = kbytes / (kms / 1e3) / 1e9
+    # roofline of the dominant kernel: HBM bytes, or tensor-core flops where those take longer at peak
+    direction = "bwd" if mean_b >= mean_f else "fwd"
+    kname, ksrc = KERNELS[("lowrank" if wl.kind == "lowrank" else "dense", direction)]
+    kms = mean_b if direction == "bwd" else mean_f
+    kbytes = prob.bytes_bwd if direction == "bwd" else prob.bytes_fwd
+    kflops = prob.flops_bwd if direction == "bwd" else prob.flops_fwd
     traffic = measured_traffic(kname, wl.name, kernel_source_digest(ksrc))
-    roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "traffic": traffic, "algorithmic_bytes": kbytes,
-            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src}
+    if kflops and kflops / (tc_peak * 1e12) > kbytes / (hbm_peak * 1e9):
+        achieved = kflops / (kms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak, "traffic": traffic, "algorithmic_flops": kflops,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops)" if peak_src == "measured" else peak_src}
+    else:
+        achieved = kbytes / (kms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic, "algorithmic_bytes": kbytes,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src}
 
     # end to end through the public API with host buffers
     e2e = None

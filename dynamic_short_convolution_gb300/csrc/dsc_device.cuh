@@ -61,33 +61,32 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// One bounded poll: the thread may sleep in the instruction until the phase
-// completes, for at most kPollSuspendNs, so a waiting warp does not keep issuing.
-constexpr uint32_t kPollSuspendNs = 100000;
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kPollSuspendNs)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
 
 // Wait until the phase with the given parity has completed, for at most
 // limit_ns of wall time (and a bounded number of polls).  Returns false on
-// timeout; never spins forever.
+// timeout; never spins forever.  After a miss the thread backs off with a short
+// sleep, so a waiting warp leaves the issue slots to the warps doing the work,
+// and it reads the wall clock only every 32 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned long long limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0; it < (1u << 28); ++it) {
+    for (uint32_t it = 1; it < (1u << 30); ++it) {
+        __nanosleep(it < 4 ? 20 : 100);
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+        if ((it & 31) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
@@ -345,10 +344,24 @@ __device__ __forceinline__ int valid_taps(int t, int T, int W, const int32_t *cu
 // the tokens jump backwards.  Same in-range guarantee for malformed offsets.
 struct DocCursor {
     int ci = -1;
-    __device__ __forceinline__ void reset() { ci = -1; }
+    int last_t = -1, last_ds = 0;  // last token asked about and the start of its sequence
+    __device__ __forceinline__ void reset()
+    {
+        ci = -1;
+        last_t = -1;
+    }
     __device__ __forceinline__ int taps(int t, int T, int W, const int32_t *cu, int n_docs)
     {
-        int ds = t - t % T;
+        // start of t's sequence: walked forward from the previous token (no division per call)
+        int ds;
+        if (last_t >= 0 && t >= last_t) {
+            ds = last_ds;
+            while (t - ds >= T) ds += T;
+        } else {
+            ds = t - t % T;
+        }
+        last_t = t;
+        last_ds = ds;
         if (cu != nullptr) {
             if (ci < 0) {
                 int lo = 0, hi = n_docs;

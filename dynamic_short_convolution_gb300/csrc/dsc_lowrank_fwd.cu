@@ -171,9 +171,9 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         if (warp == 0) {
             // ---------------- producer
             int i = it;
-            for (int v = u; v < seg_end; ++v, ++i) {
-                const int s = i % p.nstages;
-                const uint32_t ph = (i / p.nstages) & 1;
+            int s = it % p.nstages;                     // stage and its phase: stepped, not divided, per tile
+            uint32_t ph = (it / p.nstages) & 1;
+            for (int v = u; v < seg_end; ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0)) {
                 bool ok = mbar_wait(&hdr->empty[s], ph ^ 1, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
                 if (!ok) {
@@ -196,9 +196,9 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         } else if (warp == 1) {
             // ---------------- MMA issuer: acc = z . U_blk (K = R), then += 1 . bias
             int i = it;
-            for (int v = u; v < seg_end; ++v, ++i) {
-                const int s = i % p.nstages;
-                const uint32_t ph = (i / p.nstages) & 1;
+            int s = it % p.nstages;
+            uint32_t ph = (it / p.nstages) & 1;
+            for (int v = u; v < seg_end; ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0)) {
                 const int b = i & 1;
                 const uint32_t tph = (i >> 1) & 1;
                 bool ok = mbar_wait(&hdr->full[s], ph, p.wait_ns) && mbar_wait(&hdr->tmem_empty[b], tph ^ 1, p.wait_ns);
@@ -238,9 +238,9 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * (RB / 4));
             DocCursor cursor;  // this thread's token increases from tile to tile within a run
             int i = it;
-            for (int v = u; v < seg_end; ++v, ++i) {
-                const int s = i % p.nstages;
-                const uint32_t ph = (i / p.nstages) & 1;
+            int s = it % p.nstages;
+            uint32_t ph = (it / p.nstages) & 1;
+            for (int v = u; v < seg_end; ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0)) {
                 const int b = i & 1;
                 const uint32_t tph = (i >> 1) & 1;
                 bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns);
