@@ -243,8 +243,13 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             for (int v = u; v < seg_end; ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0)) {
                 const int b = i & 1;
                 const uint32_t tph = (i >> 1) & 1;
+                // valid taps of this token, worked out while the tile's accumulator is still being computed
+                const int t = (v - nb * p.n_mt) * kM + row;
+                const int nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;  // valid taps of this token
+                const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
                 bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns);
-                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+                // the other roles' failures reach this warp through the barriers it waits on
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
                     if (lane == 0) {
                         record_status(p.status, kStatusTimeout);
@@ -252,15 +257,11 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     }
                     break;
                 }
-                if (lane == 0) tma_store_wait_read<1>();  // this warp's store from two tiles ago has left buffer b
-                __syncwarp();
                 tc_fence_after();
                 const uint8_t *st = stages + s * p.stage_bytes;
                 const uint8_t *xs = st + p.x_off_in_stage;
-                const int t = (v - nb * p.n_mt) * kM + row;
-                const int nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;  // valid taps of this token
-                const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
                 uint8_t *ys = ywarp + b * (32 * (RB / 4));
+                bool ys_free = false;  // this warp's store from two tiles ago has left buffer b
                 const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
 #pragma unroll
                 for (int gi = 0; gi < GPW; ++gi) {
@@ -307,6 +308,11 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     o.y = *reinterpret_cast<uint32_t *>(&h1);
                     o.z = *reinterpret_cast<uint32_t *>(&h2);
                     o.w = *reinterpret_cast<uint32_t *>(&h3);
+                    if (!ys_free) {
+                        if (lane == 0) tma_store_wait_read<1>();
+                        __syncwarp();
+                        ys_free = true;
+                    }
                     *reinterpret_cast<uint4 *>(ys + lane * (RB / 4) + gi * 16) = o;
                 }
                 // accumulator and x tile read: hand them back; store this warp's y sub-tile
