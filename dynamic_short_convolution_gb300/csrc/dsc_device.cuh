@@ -378,19 +378,6 @@ struct DocCursor {
         const int nv = t - ds + 1;
         return nv < 1 ? 1 : (nv > W ? W : nv);
     }
-    // taps() plus the first token after t that starts a new document or sequence
-    // (so token t+k is in t's document iff t+k < *next).
-    __device__ __forceinline__ int taps_next(int t, int T, int W, const int32_t *cu, int n_docs, int *next)
-    {
-        const int nv = taps(t, T, W, cu, n_docs);
-        int nx = last_ds + T;
-        if (cu != nullptr && ci < n_docs) {
-            const int c = __ldg(cu + ci + 1);
-            if (c > t && c < nx) nx = c;
-        }
-        *next = nx;
-        return nv;
-    }
 };
 
 }  // namespace dsc
