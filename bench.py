@@ -380,6 +380,23 @@ def run_reference(args, wl, rank, world):
     return 0
 
 
+def max_over_ranks(local_ms, world, device):
+    """The job's time: the largest of the ranks' times (replicas run in lockstep, the slowest one decides)."""
+    if world <= 1:
+        return local_ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world, tokens_per_replica, steps, total_ms):
+    """Tokens processed by all replicas together per second of the job's time (weak scaling)."""
+    return world * tokens_per_replica * steps / (total_ms / 1e3)
+
+
 def workload_config(wl, world):
     shape = f"B={wl.B} T={wl.T} D={wl.D} W={wl.W}" + (f" R={wl.R}" if wl.kind == "lowrank" else f" H={wl.H}")
     return {"workload": f"{wl.name}: {shape}" + (" packed documents" if wl.packed else ""),
@@ -453,13 +470,8 @@ def main():
         raise RuntimeError("device status word set during the timed region")
 
     step_ms = [a + b for a, b in zip(f_ms, b_ms)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens = wl.B * wl.T
-    value = world * tokens * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = whole_job_tokens_per_s(world, wl.B * wl.T, args.steps, total_ms)
     mean_f, mean_b = statistics.fmean(f_ms), statistics.fmean(b_ms)
     step_bytes = prob.bytes_fwd + prob.bytes_bwd
     step_gbs = step_bytes / (total_ms / args.steps / 1e3) / 1e9
@@ -514,8 +526,6 @@ def measure_e2e(prob, steps, dev, world):
     host->device, runs fwd+bwd, and copies the results device->host, all inside the timed events."""
     import torch
 
-    import torch.distributed as dist
-
     wl = prob.wl
     names_in = ["x", "w", "dy"] if wl.kind != "lowrank" else ["x", "z", "U", "bias", "dy"]
     names_out = ["y", "dx", "dw"] if wl.kind != "lowrank" else ["y", "dx", "dz", "dU", "db"]
@@ -539,12 +549,8 @@ def measure_e2e(prob, steps, dev, world):
         torch.cuda.synchronize()
         if i >= 3:
             times.append(e0.elapsed_time(e1))
-    total = sum(times)
-    if world > 1:
-        t = torch.tensor([total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
-    value = world * wl.B * wl.T * steps / (total / 1e3)
+    total = max_over_ranks(sum(times), world, dev)
+    value = whole_job_tokens_per_s(world, wl.B * wl.T, steps, total)
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": total / steps, "steps": steps,
             "api": "dynamic_short_convolution_gb300.dsc_fwd / dsc_bwd (or dsc_lowrank_*) on pinned host copies"}
