@@ -8,7 +8,7 @@
 //
 // Work unit: 128 tokens x one block of CB channels (NB = CB*W filter columns).
 // A persistent CTA takes a contiguous run of units ordered block-major, so the
-// U block (transposed into a K-major, 128-byte-swizzled tile) stays resident
+// U block (TMA, 128-byte swizzle, read as an MN-major operand) stays resident
 // in shared memory while the CTA streams over token tiles.
 //   warp 0      TMA producer: z tile (K-major, swizzled) and the x tile with
 //               its (W-1)-token causal halo; per-token valid-tap counts
@@ -17,10 +17,9 @@
 //   warps 2..17 epilogue: tcgen05.ld of the accumulator row of one token,
 //               + bias, times the x window from shared memory, + residual,
 //               bf16 into a swizzled staging tile that one thread TMA-stores
-// Inside each group of 8 channels the filter columns are kept tap-major
-// (MMA column g*8W + k*8 + c for channel g*8+c, tap k): the 8 channels of one
-// tap are adjacent accumulator columns, so channel pairs feed packed fp32x2
-// math straight from TMEM registers.
+// The filter columns keep their natural order (column c*W + k for channel c,
+// tap k): the W taps of one channel are adjacent accumulator columns, so tap
+// pairs feed packed fp32x2 math straight from TMEM registers.
 #include "dsc_internal.h"
 #include "dsc_tcgen05.cuh"
 
@@ -42,7 +41,8 @@ struct Params {
     int n_docs;
     int BT, T, D, R, N;            // N = D * W filter columns
     int n_nb, n_mt, n_units;
-    int ksteps, kchunks;           // MMA K steps of 16; 64-wide K chunks
+    int ksteps, kchunks;           // MMA K steps of 16; 64-wide K chunks of z
+    unsigned u_bytes, u_blk_bytes; // U of a block in shared memory; one 64-column block of it
     unsigned u_off, bt_off, one_off, y_off, st_off, stage_bytes, z_bytes, x_bytes, x_off_in_stage, nv_off_in_stage;
     int nstages;
     int *status;
@@ -54,6 +54,7 @@ struct Header {
     uint64_t empty[kMaxStages];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
+    uint64_t u_full;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -71,7 +72,8 @@ __device__ __forceinline__ uint32_t swz(int row, int c)
 template <int W, int CB>
 __global__ void __launch_bounds__(lrf::kThreads, 1)
     lowrank_fwd_tc(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_x,
-                   const __grid_constant__ CUtensorMap tm_y, const lrf::Params p)
+                   const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_u,
+                   const lrf::Params p)
 {
     using namespace lrf;
     constexpr int NB = CB * W;         // filter columns per block (MMA N)
@@ -79,23 +81,19 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     constexpr int GROUPS = CB / 8;     // 8-channel groups per block
     constexpr int GPW = GROUPS / 4;    // groups per epilogue warp (four warps per lane quadrant)
     static_assert(NB % 16 == 0 && NB <= 256, "MMA N");
-    constexpr uint32_t IDESC = idesc_bf16_f32(kM, NB);
+    constexpr uint32_t IDESC = idesc_bf16_f32(kM, NB, false, true);        // A z K-major, B U MN-major
+    constexpr uint32_t IDESC_BIAS = idesc_bf16_f32(kM, NB, false, false);  // A ones, B bias tile, both K-major
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Header *hdr = reinterpret_cast<Header *>(smem_raw);
     uint8_t *base = smem_raw + 1024;
     base += (1024u - (smem_u32(base) & 1023u)) & 1023u;
-    uint8_t *u_s = base + p.u_off;       // [kchunks][NB rows][128 B], 128-B swizzled, K-major
+    uint8_t *u_s = base + p.u_off;       // [NB/64 blocks][Rp rows][128 B]: U of the block, 128-B swizzled
     uint8_t *bt_s = base + p.bt_off;     // bias as an MMA B tile: [NB rows][16 K], no swizzle
     uint8_t *one_s = base + p.one_off;   // all-ones MMA A tile [128 rows][16 K]
     uint8_t *y_s = base + p.y_off;       // per epilogue warp: 2 x [32 rows][RB/4] staging for its own stores
     uint8_t *stages = base + p.st_off;
 
-    // block column n = (g*8 + c)*W + k  ->  MMA column g*8W + k*8 + c (tap-major inside a group)
-    auto tap_major = [](int n) {
-        const int g = n / (8 * W), rem = n - g * (8 * W);
-        return g * (8 * W) + (rem % W) * 8 + rem / W;
-    };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nstages; ++s) {
@@ -106,6 +104,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             mbar_init(&hdr->tmem_full[b], 1);
             mbar_init(&hdr->tmem_empty[b], kEpiWarps);
         }
+        mbar_init(&hdr->u_full, 1);
         hdr->abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -129,28 +128,19 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
 #pragma unroll
     for (int s = 0; s < kMaxStages; ++s) issued_last[s] = -1;
     int mma_last = -1;      // last tile whose MMAs were committed (MMA thread)
+    int seg = 0;            // runs of tiles (U block loads)
 
     for (int u = u_begin; u < u_end;) {
         const int nb = u / p.n_mt;
         const int seg_end = min(u_end, (nb + 1) * p.n_mt);
 
-        // ---- the block's filter generator: U[:, nb*NB .. +NB) transposed to K-major, and the bias
-        //      as an extra K step (exact bf16 hi + lo pair) that the all-ones A tile adds in
+        // ---- the block's filter generator: U[:, nb*NB .. +NB) by TMA (rows past R arrive as zeros), and the
+        //      bias as an extra K step (exact bf16 hi + lo pair) that the all-ones A tile adds in
         {
-            const int nK = p.kchunks * 64;
-            const int items = nK * (NB / 8);
-            for (int idx = threadIdx.x; idx < items; idx += blockDim.x) {
-                const int n8 = idx / nK, r = idx - n8 * nK;
-                const int n = n8 * 8, gn = nb * NB + n;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (r < p.R && gn < p.N) v = *reinterpret_cast<const uint4 *>(p.U + static_cast<size_t>(r) * p.N + gn);
-                const uint16_t *e = reinterpret_cast<const uint16_t *>(&v);
-                const int a = r >> 6, c = (r & 63) >> 3, o = (r & 7) * 2;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int row = tap_major(n + j);  // MMA column of block column n+j
-                    *reinterpret_cast<uint16_t *>(u_s + a * (NB * 128) + row * 128 + ((c ^ (row & 7)) << 4) + o) = e[j];
-                }
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(&hdr->u_full, p.u_bytes);
+                for (int blk = 0; blk < (NB + 63) / 64; ++blk)
+                    tma_load_2d(u_s + blk * p.u_blk_bytes, &tm_u, &hdr->u_full, nb * NB + blk * 64, 0);
             }
             for (int n = threadIdx.x; n < NB; n += blockDim.x) {
                 const int gn = nb * NB + n;
@@ -158,9 +148,8 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv)));
                 const uint32_t lo =
                     static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv - __uint_as_float(hi << 16))));
-                const int row = tap_major(n);
-                // core matrices of 8 rows x 16 B: K-half 0 at ((row/8)*2)*128, K-half 1 next to it
-                uint8_t *cm = bt_s + ((row >> 3) * 2) * 128 + (row & 7) * 16;
+                // core matrices of 8 rows x 16 B: K-half 0 at ((n/8)*2)*128, K-half 1 next to it
+                uint8_t *cm = bt_s + ((n >> 3) * 2) * 128 + (n & 7) * 16;
                 *reinterpret_cast<uint4 *>(cm) = make_uint4(hi | (lo << 16), 0u, 0u, 0u);
                 *reinterpret_cast<uint4 *>(cm + 128) = make_uint4(0u, 0u, 0u, 0u);
             }
@@ -195,6 +184,12 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             }
         } else if (warp == 1) {
             // ---------------- MMA issuer: acc = z . U_blk (K = R), then += 1 . bias
+            bool u_ok = mbar_wait(&hdr->u_full, seg & 1, p.wait_ns);
+            u_ok = __all_sync(0xffffffffu, u_ok);
+            if (!u_ok && lane == 0) {
+                record_status(p.status, kStatusTimeout);
+                *abort_flag = 1;
+            }
             int i = it;
             int s = it % p.nstages;
             uint32_t ph = (it / p.nstages) & 1;
@@ -216,12 +211,15 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     const uint32_t us = smem_u32(u_s);
                     const uint32_t d = tmem + b * 256;
                     for (int ks = 0; ks < p.ksteps; ++ks) {
+                        // A: z, K-major, 64-column chunks; B: U, MN-major, 16 rows of R per K step, 64-column
+                        // blocks p.u_blk_bytes apart
                         const int a = ks >> 2, kk = ks & 3;
                         const uint64_t ad = sdesc_kmajor_sw128(zs + a * 16384 + kk * 32);
-                        const uint64_t bd = sdesc_kmajor_sw128(us + a * (NB * 128) + kk * 32);
+                        const uint64_t bd = sdesc(us + ks * 2048, p.u_blk_bytes, 1024, 2);
                         umma_bf16(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
                     }
-                    umma_bf16(d, sdesc(smem_u32(one_s), 128, 256, 0), sdesc(smem_u32(bt_s), 128, 256, 0), IDESC, 1u);
+                    umma_bf16(d, sdesc(smem_u32(one_s), 128, 256, 0), sdesc(smem_u32(bt_s), 128, 256, 0), IDESC_BIAS,
+                              1u);
                     umma_commit(&hdr->empty[s]);
                     umma_commit(&hdr->tmem_full[b]);
                     mma_last = i;
@@ -266,40 +264,40 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
 #pragma unroll
                 for (int gi = 0; gi < GPW; ++gi) {
                     const int g = h * GPW + gi;  // 8-channel group
-                    uint32_t acc[8 * W];         // acc[k*8 + c]: tap k of channel g*8 + c
+                    uint32_t acc[8 * W];         // acc[c*W + k]: tap k of channel g*8 + c
                     tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
-                    float2 out[4];
-                    {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + W - 1, g));
-                        out[0] = bf16x2_to_f2(raw.x);  // residual: x of the token itself
-                        out[1] = bf16x2_to_f2(raw.y);
-                        out[2] = bf16x2_to_f2(raw.z);
-                        out[3] = bf16x2_to_f2(raw.w);
-                    }
-                    const float2 x0[4] = {out[0], out[1], out[2], out[3]};
-                    tmem_ld_wait();
+                    uint32_t xw[W][4];           // x~ rows row-k of the group's 8 channels, bf16 pairs
 #pragma unroll
                     for (int k = 0; k < W; ++k) {
-                        float2 xk[4];
-                        if (k == 0) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
+                        const bool keep = full_taps || k < nv;  // x~ is zero before the document start
+                        xw[k][0] = keep ? raw.x : 0u;
+                        xw[k][1] = keep ? raw.y : 0u;
+                        xw[k][2] = keep ? raw.z : 0u;
+                        xw[k][3] = keep ? raw.w : 0u;
+                    }
+                    tmem_ld_wait();
+                    float2 out[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) xk[e] = x0[e];
-                        } else {
-                            const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
-                            xk[0] = bf16x2_to_f2(raw.x);
-                            xk[1] = bf16x2_to_f2(raw.y);
-                            xk[2] = bf16x2_to_f2(raw.z);
-                            xk[3] = bf16x2_to_f2(raw.w);
-                            if (!full_taps && k >= nv) {  // x~ is zero before the document start
+                    for (int e = 0; e < 4; ++e) {
+                        float y2[2];
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) xk[e] = make_float2(0.f, 0.f);
-                            }
+                        for (int h2 = 0; h2 < 2; ++h2) {  // channel c = 2e + h2
+                            const int c = 2 * e + h2;
+                            auto xv = [&](int k) {
+                                const uint32_t w2 = xw[k][e];
+                                return __uint_as_float(h2 ? (w2 & 0xffff0000u) : (w2 << 16));
+                            };
+                            // residual + sum_k acc_k * x~_k, taps paired for packed fp32x2 arithmetic
+                            float2 sum = make_float2(xv(0), 0.f);
+#pragma unroll
+                            for (int k = 0; k + 1 < W; k += 2)
+                                sum = fma2(make_float2(__uint_as_float(acc[c * W + k]), __uint_as_float(acc[c * W + k + 1])),
+                                           make_float2(xv(k), xv(k + 1)), sum);
+                            if constexpr (W % 2 == 1) sum.x = fmaf(__uint_as_float(acc[c * W + W - 1]), xv(W - 1), sum.x);
+                            y2[h2] = sum.x + sum.y;
                         }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            out[e] = fma2(make_float2(__uint_as_float(acc[k * 8 + 2 * e]),
-                                                      __uint_as_float(acc[k * 8 + 2 * e + 1])),
-                                          xk[e], out[e]);
+                        out[e] = make_float2(y2[0], y2[1]);
                     }
                     uint4 o;
                     __nv_bfloat162 h0 = __float22bfloat162_rn(out[0]), h1 = __float22bfloat162_rn(out[1]);
@@ -330,6 +328,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         }
         it += seg_end - u;
         u = seg_end;
+        ++seg;
         __syncthreads();
         if (*abort_flag) break;
     }
@@ -375,7 +374,9 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     // shared memory: [header 1 KB][align slack 1 KB][U][bias tile][ones tile][y staging x2][stages]
     unsigned off = 0;
     p.u_off = off;
-    off += p.kchunks * NB * 128;
+    p.u_blk_bytes = p.ksteps * 16 * 128;  // rows R rounded up to 16 (TMA fills the rest with zeros)
+    p.u_bytes = ((NB + 63) / 64) * p.u_blk_bytes;
+    off += p.u_bytes;
     p.bt_off = align_up(off, 1024);
     off = p.bt_off + NB * 32;
     p.one_off = align_up(off, 1024);
@@ -396,7 +397,7 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     p.status = device_status_word();
     p.wait_ns = wait_limit_ns();
 
-    CUtensorMap tm_z, tm_x, tm_y;
+    CUtensorMap tm_z, tm_x, tm_y, tm_u;
     const CUtensorMapSwizzle sw = RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const unsigned long long BT = static_cast<unsigned long long>(p.BT);
     if (!encode_tmap_2d(&tm_z, a.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.R, BT, static_cast<unsigned long long>(a.R) * 2,
@@ -404,13 +405,15 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
         !encode_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.D, BT, static_cast<unsigned long long>(a.D) * 2,
                         CB, XR, sw) ||
         !encode_tmap_2d(&tm_y, a.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.D, BT, static_cast<unsigned long long>(a.D) * 2,
-                        CB / 4, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+                        CB / 4, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_2d(&tm_u, a.U, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.N, a.R, static_cast<unsigned long long>(p.N) * 2,
+                        64, p.ksteps * 16, CU_TENSOR_MAP_SWIZZLE_128B))
         return DSC_ERR_CUDA;
     auto kern = lowrank_fwd_tc<W, CB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return DSC_ERR_CUDA;
     int grid = dev.sm_count < p.n_units ? dev.sm_count : p.n_units;
-    kern<<<grid, kThreads, smem, a.stream>>>(tm_z, tm_x, tm_y, p);
+    kern<<<grid, kThreads, smem, a.stream>>>(tm_z, tm_x, tm_y, tm_u, p);
     return launched();
 }
 
