@@ -270,11 +270,16 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < W; ++k) {
                         const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
-                        const bool keep = full_taps || k < nv;  // x~ is zero before the document start
-                        xw[k][0] = keep ? raw.x : 0u;
-                        xw[k][1] = keep ? raw.y : 0u;
-                        xw[k][2] = keep ? raw.z : 0u;
-                        xw[k][3] = keep ? raw.w : 0u;
+                        xw[k][0] = raw.x;
+                        xw[k][1] = raw.y;
+                        xw[k][2] = raw.z;
+                        xw[k][3] = raw.w;
+                    }
+                    if (!full_taps) {  // x~ is zero before the document start (warp-uniform branch)
+#pragma unroll
+                        for (int k = 1; k < W; ++k)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) xw[k][e] = k < nv ? xw[k][e] : 0u;
                     }
                     tmem_ld_wait();
                     float2 out[4];
