@@ -226,6 +226,7 @@ dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const fl
 {
     dsc_status s = lowrank_check(x, z, U, bias, B, T, D, W, R, dt, cu_seqlens, n_docs);
     if (s != DSC_OK) return s;
+    if (R % 16 != 0 || R > 64) return DSC_ERR_UNSUPPORTED;  // the backward's TMEM plan: dz is R <= 64 columns
     if (!dy || !dx || !dz || !dU || !db) return DSC_ERR_INVALID_ARG;
     if (!aligned16(dy) || !aligned16(dx) || !aligned16(dz) || !aligned16(dU) || !aligned16(db))
         return DSC_ERR_UNSUPPORTED;

@@ -132,7 +132,9 @@ size_t dsc_lowrank_bwd_workspace_bytes(int B, int T, int D, int W, int R);
  *     db[n]   = sum_t G[t,n]               (fp32 [D*W])
  *   `workspace` must hold dsc_lowrank_bwd_workspace_bytes() bytes of device
  *   memory, 256-byte aligned (may be NULL when that size is 0); its contents on
- *   entry are ignored.  Same requirements as dsc_lowrank_fwd.
+ *   entry are ignored.  Same requirements as dsc_lowrank_fwd, and in addition
+ *   R % 16 == 0 and R <= 64 (other ranks return DSC_ERR_UNSUPPORTED before
+ *   anything is launched).
  */
 dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const float *bias, const void *dy, void *dx,
                            void *dz, float *dU, float *db, void *workspace, int B, int T, int D, int W, int R,

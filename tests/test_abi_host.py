@@ -64,6 +64,10 @@ def test_rejects_bad_arguments_before_any_launch(L):
     assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 16, f32, None, 0, None) == 2
     assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 256, bf16, None, 0, None) == 2
     assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 0, bf16, None, 0, None) == 1
+    # low-rank backward: R a multiple of 16 up to 64 only
+    for r in (8, 24, 80, 128):
+        assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, p, 1, 8, 64, 4, r, bf16, None, 0, None) == 2
+    assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, 16, bf16, None, 0, None) == 1  # no workspace
     assert L.dsc_validate_cu_seqlens(None, 3, 1, 8, None) == 1
 
 
