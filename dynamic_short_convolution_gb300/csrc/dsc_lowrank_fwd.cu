@@ -54,7 +54,7 @@ struct Header {
     uint64_t empty[kMaxStages];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t u_full;
+    uint64_t u_full, u_free;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -105,11 +105,17 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             mbar_init(&hdr->tmem_empty[b], kEpiWarps);
         }
         mbar_init(&hdr->u_full, 1);
+        mbar_init(&hdr->u_free, 1);
         hdr->abort_flag = 0;
         fence_mbarrier_init();
     }
     for (int i = threadIdx.x; i < kM * 16 / 2; i += blockDim.x)
         reinterpret_cast<uint32_t *>(one_s)[i] = 0x3F803F80u;  // bf16 1.0 pairs
+    // bias B tile, core matrices of 8 rows x 16 B: column n's first K pair (at ((n/8)*2)*128 + (n%8)*16) holds
+    // the bias as an exact bf16 hi + lo pair, the rest of its K = 16 is zero.  Only the pair changes per block.
+    for (int i = threadIdx.x; i < NB * 2; i += blockDim.x)
+        reinterpret_cast<uint4 *>(bt_s)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(&hdr->tmem_base, kTmemCols);
         tmem_relinquish();
@@ -123,221 +129,241 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     const int u_begin = static_cast<int>(static_cast<long long>(blockIdx.x) * p.n_units / gridDim.x);
     const int u_end = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.n_units / gridDim.x);
 
-    int it = 0;             // tiles through the stage ring (all roles count the same)
     int issued_last[kMaxStages];
 #pragma unroll
     for (int s = 0; s < kMaxStages; ++s) issued_last[s] = -1;
     int mma_last = -1;      // last tile whose MMAs were committed (MMA thread)
-    int seg = 0;            // runs of tiles (U block loads)
+    int seg = 0;            // filter-generator loads so far (MMA warp)
+    bool u_pending = false; // MMA warp: a U load is in flight and was not seen to complete
 
-    for (int u = u_begin; u < u_end;) {
-        const int nb = u / p.n_mt;
-        const int seg_end = min(u_end, (nb + 1) * p.n_mt);
-
-        // ---- the block's filter generator: U[:, nb*NB .. +NB) by TMA (rows past R arrive as zeros), and the
-        //      bias as an extra K step (exact bf16 hi + lo pair) that the all-ones A tile adds in
-        {
-            if (threadIdx.x == 0) {
-                mbar_arrive_expect_tx(&hdr->u_full, p.u_bytes);
-                for (int blk = 0; blk < (NB + 63) / 64; ++blk)
-                    tma_load_2d(u_s + blk * p.u_blk_bytes, &tm_u, &hdr->u_full, nb * NB + blk * 64, 0);
+    if (warp == 0) {
+        // ---------------- producer: streams z and x tiles from the first cycle, across block changes
+        int i = 0;
+        int s = 0;                                  // stage and its phase: stepped, not divided, per tile
+        uint32_t ph = 0;
+        int nb = u_begin / p.n_mt, mt = u_begin - nb * p.n_mt;
+        for (int v = u_begin; v < u_end;
+             ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0), mt = (mt + 1 == p.n_mt) ? 0 : mt + 1,
+                 nb += (mt == 0)) {
+            bool ok = mbar_wait(&hdr->empty[s], ph ^ 1, p.wait_ns);
+            ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+            if (!ok) {
+                if (lane == 0) {
+                    record_status(p.status, kStatusTimeout);
+                    *abort_flag = 1;
+                }
+                break;
             }
-            for (int n = threadIdx.x; n < NB; n += blockDim.x) {
-                const int gn = nb * NB + n;
-                const float bv = gn < p.N ? p.bias[gn] : 0.f;
-                const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv)));
-                const uint32_t lo =
-                    static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv - __uint_as_float(hi << 16))));
-                // core matrices of 8 rows x 16 B: K-half 0 at ((n/8)*2)*128, K-half 1 next to it
-                uint8_t *cm = bt_s + ((n >> 3) * 2) * 128 + (n & 7) * 16;
-                *reinterpret_cast<uint4 *>(cm) = make_uint4(hi | (lo << 16), 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(cm + 128) = make_uint4(0u, 0u, 0u, 0u);
+            const int t0 = mt * kM;
+            uint8_t *st = stages + s * p.stage_bytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&hdr->full[s], p.z_bytes + p.x_bytes);
+                for (int a = 0; a < p.kchunks; ++a) tma_load_2d(st + a * 16384, &tm_z, &hdr->full[s], a * 64, t0);
+                tma_load_2d(st + p.x_off_in_stage, &tm_x, &hdr->full[s], nb * CB, t0 - (W - 1));
+                issued_last[s] = i;
             }
-            fence_proxy_async_smem();
         }
-        __syncthreads();
-
-        if (warp == 0) {
-            // ---------------- producer
-            int i = it;
-            int s = it % p.nstages;                     // stage and its phase: stepped, not divided, per tile
-            uint32_t ph = (it / p.nstages) & 1;
-            for (int v = u; v < seg_end; ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0)) {
-                bool ok = mbar_wait(&hdr->empty[s], ph ^ 1, p.wait_ns);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: acc = z . U_blk (K = R), then += 1 . bias.  This warp also loads each
+        // block's filter generator, once the previous block's MMAs have completed, so that the producer never
+        // stops streaming and no other warp waits at a block change.
+        int i = 0;
+        int s = 0;
+        uint32_t ph = 0;
+        int nb = u_begin / p.n_mt, mt = u_begin - nb * p.n_mt;
+        int cur_nb = -1;
+        for (int v = u_begin; v < u_end;
+             ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0), mt = (mt + 1 == p.n_mt) ? 0 : mt + 1,
+                 nb += (mt == 0)) {
+            if (nb != cur_nb) {
+                // U[:, nb*NB .. +NB) by TMA (rows past R arrive as zeros); the bias as an extra K step (exact
+                // bf16 hi + lo pair) that the all-ones A tile adds in
+                float bv[(NB + 31) / 32];
+#pragma unroll
+                for (int j = 0; j < (NB + 31) / 32; ++j) {
+                    const int n = lane + 32 * j, gn = nb * NB + n;
+                    bv[j] = (n < NB && gn < p.N) ? p.bias[gn] : 0.f;
+                }
+                bool ok = true;
+                if (cur_nb >= 0) {  // the previous block's MMAs still read U and the bias tile
+                    if (lane == 0) umma_commit(&hdr->u_free);
+                    __syncwarp();
+                    ok = mbar_wait(&hdr->u_free, (seg - 1) & 1, p.wait_ns);
+                }
                 ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        record_status(p.status, kStatusTimeout);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-                const int mt = v - nb * p.n_mt;
-                const int t0 = mt * kM;
-                uint8_t *st = stages + s * p.stage_bytes;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&hdr->full[s], p.z_bytes + p.x_bytes);
-                    for (int a = 0; a < p.kchunks; ++a) tma_load_2d(st + a * 16384, &tm_z, &hdr->full[s], a * 64, t0);
-                    tma_load_2d(st + p.x_off_in_stage, &tm_x, &hdr->full[s], nb * CB, t0 - (W - 1));
-                    issued_last[s] = i;
-                }
-            }
-        } else if (warp == 1) {
-            // ---------------- MMA issuer: acc = z . U_blk (K = R), then += 1 . bias
-            bool u_ok = mbar_wait(&hdr->u_full, seg & 1, p.wait_ns);
-            u_ok = __all_sync(0xffffffffu, u_ok);
-            if (!u_ok && lane == 0) {
-                record_status(p.status, kStatusTimeout);
-                *abort_flag = 1;
-            }
-            int i = it;
-            int s = it % p.nstages;
-            uint32_t ph = (it / p.nstages) & 1;
-            for (int v = u; v < seg_end; ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0)) {
-                const int b = i & 1;
-                const uint32_t tph = (i >> 1) & 1;
-                bool ok = mbar_wait(&hdr->full[s], ph, p.wait_ns) && mbar_wait(&hdr->tmem_empty[b], tph ^ 1, p.wait_ns);
-                ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        record_status(p.status, kStatusTimeout);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t zs = smem_u32(stages + s * p.stage_bytes);
-                    const uint32_t us = smem_u32(u_s);
-                    const uint32_t d = tmem + b * 256;
-                    for (int ks = 0; ks < p.ksteps; ++ks) {
-                        // A: z, K-major, 64-column chunks; B: U, MN-major, 16 rows of R per K step, 64-column
-                        // blocks p.u_blk_bytes apart
-                        const int a = ks >> 2, kk = ks & 3;
-                        const uint64_t ad = sdesc_kmajor_sw128(zs + a * 16384 + kk * 32);
-                        const uint64_t bd = sdesc(us + ks * 2048, p.u_blk_bytes, 1024, 2);
-                        umma_bf16(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
-                    }
-                    umma_bf16(d, sdesc(smem_u32(one_s), 128, 256, 0), sdesc(smem_u32(bt_s), 128, 256, 0), IDESC_BIAS,
-                              1u);
-                    umma_commit(&hdr->empty[s]);
-                    umma_commit(&hdr->tmem_full[b]);
-                    mma_last = i;
-                }
-                __syncwarp();
-            }
-        } else {
-            // ---------------- epilogue: y = x + sum_k acc_k * x~_k (the bias is inside acc).  Each warp
-            // owns 32 tokens x CB/4 channels of the tile and stores them itself (TMA, private double
-            // buffer), so no warp ever waits for another one.
-            const int q = warp & 3;                          // TMEM lane quadrant
-            const int h = (warp - kEpiWarp0) >> 2;           // which quarter of the channel groups
-            const int row = q * 32 + lane;                   // token within the tile
-            uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * (RB / 4));
-            DocCursor cursor;  // this thread's token increases from tile to tile within a run
-            int i = it;
-            int s = it % p.nstages;
-            uint32_t ph = (it / p.nstages) & 1;
-            for (int v = u; v < seg_end; ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0)) {
-                const int b = i & 1;
-                const uint32_t tph = (i >> 1) & 1;
-                // valid taps of this token, worked out while the tile's accumulator is still being computed
-                const int t = (v - nb * p.n_mt) * kM + row;
-                const int nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;  // valid taps of this token
-                const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
-                bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns);
-                // the other roles' failures reach this warp through the barriers it waits on
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) {
-                    if (lane == 0) {
-                        record_status(p.status, kStatusTimeout);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-                tc_fence_after();
-                const uint8_t *st = stages + s * p.stage_bytes;
-                const uint8_t *xs = st + p.x_off_in_stage;
-                uint8_t *ys = ywarp + b * (32 * (RB / 4));
-                bool ys_free = false;  // this warp's store from two tiles ago has left buffer b
-                const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
+                if (ok) {
 #pragma unroll
-                for (int gi = 0; gi < GPW; ++gi) {
-                    const int g = h * GPW + gi;  // 8-channel group
-                    uint32_t acc[8 * W];         // acc[c*W + k]: tap k of channel g*8 + c
-                    tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
-                    uint32_t xw[W][4];           // x~ rows row-k of the group's 8 channels, bf16 pairs
-#pragma unroll
-                    for (int k = 0; k < W; ++k) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
-                        xw[k][0] = raw.x;
-                        xw[k][1] = raw.y;
-                        xw[k][2] = raw.z;
-                        xw[k][3] = raw.w;
-                    }
-                    if (!full_taps) {  // x~ is zero before the document start (warp-uniform branch)
-#pragma unroll
-                        for (int k = 1; k < W; ++k)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) xw[k][e] = k < nv ? xw[k][e] : 0u;
-                    }
-                    tmem_ld_wait();
-                    float2 out[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float y2[2];
-#pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {  // channel c = 2e + h2
-                            const int c = 2 * e + h2;
-                            auto xv = [&](int k) {
-                                const uint32_t w2 = xw[k][e];
-                                return __uint_as_float(h2 ? (w2 & 0xffff0000u) : (w2 << 16));
-                            };
-                            // residual + sum_k acc_k * x~_k, taps paired for packed fp32x2 arithmetic
-                            float2 sum = make_float2(xv(0), 0.f);
-#pragma unroll
-                            for (int k = 0; k + 1 < W; k += 2)
-                                sum = fma2(make_float2(__uint_as_float(acc[c * W + k]), __uint_as_float(acc[c * W + k + 1])),
-                                           make_float2(xv(k), xv(k + 1)), sum);
-                            if constexpr (W % 2 == 1) sum.x = fmaf(__uint_as_float(acc[c * W + W - 1]), xv(W - 1), sum.x);
-                            y2[h2] = sum.x + sum.y;
+                    for (int j = 0; j < (NB + 31) / 32; ++j) {
+                        const int n = lane + 32 * j;
+                        if (n < NB) {
+                            const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bv[j])));
+                            const uint32_t lo = static_cast<uint32_t>(
+                                __bfloat16_as_ushort(__float2bfloat16_rn(bv[j] - __uint_as_float(hi << 16))));
+                            *reinterpret_cast<uint32_t *>(bt_s + ((n >> 3) * 2) * 128 + (n & 7) * 16) = hi | (lo << 16);
                         }
-                        out[e] = make_float2(y2[0], y2[1]);
                     }
-                    uint4 o;
-                    __nv_bfloat162 h0 = __float22bfloat162_rn(out[0]), h1 = __float22bfloat162_rn(out[1]);
-                    __nv_bfloat162 h2 = __float22bfloat162_rn(out[2]), h3 = __float22bfloat162_rn(out[3]);
-                    o.x = *reinterpret_cast<uint32_t *>(&h0);
-                    o.y = *reinterpret_cast<uint32_t *>(&h1);
-                    o.z = *reinterpret_cast<uint32_t *>(&h2);
-                    o.w = *reinterpret_cast<uint32_t *>(&h3);
-                    if (!ys_free) {
-                        if (lane == 0) tma_store_wait_read<1>();
-                        __syncwarp();
-                        ys_free = true;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&hdr->u_full, p.u_bytes);
+                        for (int blk = 0; blk < (NB + 63) / 64; ++blk)
+                            tma_load_2d(u_s + blk * p.u_blk_bytes, &tm_u, &hdr->u_full, nb * NB + blk * 64, 0);
                     }
-                    *reinterpret_cast<uint4 *>(ys + lane * (RB / 4) + gi * 16) = o;
+                    u_pending = true;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&hdr->u_full, seg & 1, p.wait_ns));
+                    if (ok) u_pending = false;
                 }
-                // accumulator and x tile read: hand them back; store this warp's y sub-tile
-                tc_fence_before();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&hdr->tmem_empty[b]);
-                    mbar_arrive(&hdr->empty[s]);
-                    const int t0 = (v - nb * p.n_mt) * kM;
-                    tma_store_2d(&tm_y, ys, nb * CB + h * (CB / 4), t0 + q * 32);
-                    tma_store_commit();
+                ++seg;
+                cur_nb = nb;
+                if (!ok) {
+                    if (lane == 0) {
+                        record_status(p.status, kStatusTimeout);
+                        *abort_flag = 1;
+                    }
+                    break;
                 }
             }
+            const int b = i & 1;
+            const uint32_t tph = (i >> 1) & 1;
+            bool ok = mbar_wait(&hdr->full[s], ph, p.wait_ns) && mbar_wait(&hdr->tmem_empty[b], tph ^ 1, p.wait_ns);
+            ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
+            if (!ok) {
+                if (lane == 0) {
+                    record_status(p.status, kStatusTimeout);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t zs = smem_u32(stages + s * p.stage_bytes);
+                const uint32_t us = smem_u32(u_s);
+                const uint32_t d = tmem + b * 256;
+                for (int ks = 0; ks < p.ksteps; ++ks) {
+                    // A: z, K-major, 64-column chunks; B: U, MN-major, 16 rows of R per K step, 64-column
+                    // blocks p.u_blk_bytes apart
+                    const int a = ks >> 2, kk = ks & 3;
+                    const uint64_t ad = sdesc_kmajor_sw128(zs + a * 16384 + kk * 32);
+                    const uint64_t bd = sdesc(us + ks * 2048, p.u_blk_bytes, 1024, 2);
+                    umma_bf16(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
+                }
+                umma_bf16(d, sdesc(smem_u32(one_s), 128, 256, 0), sdesc(smem_u32(bt_s), 128, 256, 0), IDESC_BIAS,
+                          1u);
+                umma_commit(&hdr->empty[s]);
+                umma_commit(&hdr->tmem_full[b]);
+                mma_last = i;
+            }
+            __syncwarp();
         }
-        it += seg_end - u;
-        u = seg_end;
-        ++seg;
-        __syncthreads();
-        if (*abort_flag) break;
+    } else {
+        // ---------------- epilogue: y = x + sum_k acc_k * x~_k (the bias is inside acc).  Each warp
+        // owns 32 tokens x CB/4 channels of the tile and stores them itself (TMA, private double
+        // buffer), so no warp ever waits for another one.
+        const int q = warp & 3;                          // TMEM lane quadrant
+        const int h = (warp - kEpiWarp0) >> 2;           // which quarter of the channel groups
+        const int row = q * 32 + lane;                   // token within the tile
+        uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * (RB / 4));
+        DocCursor cursor;  // this thread's token increases from tile to tile within a block
+        int i = 0;
+        int s = 0;
+        uint32_t ph = 0;
+        int nb = u_begin / p.n_mt, mt = u_begin - nb * p.n_mt;
+        for (int v = u_begin; v < u_end;
+             ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0), mt = (mt + 1 == p.n_mt) ? 0 : mt + 1,
+                 nb += (mt == 0)) {
+            if (mt == 0) cursor.reset();  // a new block starts again from the first token
+            const int b = i & 1;
+            const uint32_t tph = (i >> 1) & 1;
+            // valid taps of this token, worked out while the tile's accumulator is still being computed
+            const int t = mt * kM + row;
+            const int nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;  // valid taps of this token
+            const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
+            bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns);
+            // the other roles' failures reach this warp through the barriers it waits on
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) {
+                    record_status(p.status, kStatusTimeout);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            const uint8_t *st = stages + s * p.stage_bytes;
+            const uint8_t *xs = st + p.x_off_in_stage;
+            uint8_t *ys = ywarp + b * (32 * (RB / 4));
+            bool ys_free = false;  // this warp's store from two tiles ago has left buffer b
+            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
+#pragma unroll
+            for (int gi = 0; gi < GPW; ++gi) {
+                const int g = h * GPW + gi;  // 8-channel group
+                uint32_t acc[8 * W];         // acc[c*W + k]: tap k of channel g*8 + c
+                tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
+                uint32_t xw[W][4];           // x~ rows row-k of the group's 8 channels, bf16 pairs
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
+                    xw[k][0] = raw.x;
+                    xw[k][1] = raw.y;
+                    xw[k][2] = raw.z;
+                    xw[k][3] = raw.w;
+                }
+                if (!full_taps) {  // x~ is zero before the document start (warp-uniform branch)
+#pragma unroll
+                    for (int k = 1; k < W; ++k)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) xw[k][e] = k < nv ? xw[k][e] : 0u;
+                }
+                tmem_ld_wait();
+                float2 out[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float y2[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {  // channel c = 2e + h2
+                        const int c = 2 * e + h2;
+                        auto xv = [&](int k) {
+                            const uint32_t w2 = xw[k][e];
+                            return __uint_as_float(h2 ? (w2 & 0xffff0000u) : (w2 << 16));
+                        };
+                        // residual + sum_k acc_k * x~_k, taps paired for packed fp32x2 arithmetic
+                        float2 sum = make_float2(xv(0), 0.f);
+#pragma unroll
+                        for (int k = 0; k + 1 < W; k += 2)
+                            sum = fma2(make_float2(__uint_as_float(acc[c * W + k]), __uint_as_float(acc[c * W + k + 1])),
+                                       make_float2(xv(k), xv(k + 1)), sum);
+                        if constexpr (W % 2 == 1) sum.x = fmaf(__uint_as_float(acc[c * W + W - 1]), xv(W - 1), sum.x);
+                        y2[h2] = sum.x + sum.y;
+                    }
+                    out[e] = make_float2(y2[0], y2[1]);
+                }
+                uint4 o;
+                __nv_bfloat162 h0 = __float22bfloat162_rn(out[0]), h1 = __float22bfloat162_rn(out[1]);
+                __nv_bfloat162 h2 = __float22bfloat162_rn(out[2]), h3 = __float22bfloat162_rn(out[3]);
+                o.x = *reinterpret_cast<uint32_t *>(&h0);
+                o.y = *reinterpret_cast<uint32_t *>(&h1);
+                o.z = *reinterpret_cast<uint32_t *>(&h2);
+                o.w = *reinterpret_cast<uint32_t *>(&h3);
+                if (!ys_free) {
+                    if (lane == 0) tma_store_wait_read<1>();
+                    __syncwarp();
+                    ys_free = true;
+                }
+                *reinterpret_cast<uint4 *>(ys + lane * (RB / 4) + gi * 16) = o;
+            }
+            // accumulator and x tile read: hand them back; store this warp's y sub-tile
+            tc_fence_before();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&hdr->tmem_empty[b]);
+                mbar_arrive(&hdr->empty[s]);
+                const int t0 = mt * kM;
+                tma_store_2d(&tm_y, ys, nb * CB + h * (CB / 4), t0 + q * 32);
+                tma_store_commit();
+            }
+        }
     }
-
     // ---- teardown: no copy or MMA of this CTA may still be in flight
     if (warp == 0 && lane == 0 && *abort_flag) {
         for (int s = 0; s < p.nstages; ++s)
@@ -345,6 +371,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     }
     if (warp == 1 && lane == 0 && mma_last >= 0)
         (void)mbar_wait(&hdr->tmem_full[mma_last & 1], (mma_last >> 1) & 1, kDrainLimitNs);
+    if (warp == 1 && lane == 0 && u_pending) (void)mbar_wait(&hdr->u_full, (seg - 1) & 1, kDrainLimitNs);
     if (warp >= kEpiWarp0 && lane == 0) tma_store_wait_all<0>();
     tc_fence_before();
     __syncthreads();

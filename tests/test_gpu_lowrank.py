@@ -74,6 +74,22 @@ def test_lowrank_fwd_full_size_sampled(dsc, oracle_mod):
     assert torch.isfinite(y).all()
 
 
+# Packed documents on more units than SMs: every persistent CTA walks a run of several tiles that
+# crosses from one channel block to the next (its filter generator is reloaded mid-run).
+MULTI_RUN = (2, 1536, 1024, 4, 64)
+
+
+def test_lowrank_fwd_runs_across_blocks(dsc, oracle_mod):
+    B, T, D, W, R = MULTI_RUN
+    wl = inputs.custom(B, T, D, W, R=R, dtype="bf16", seed_id=481, packed=True, doc_min=1, doc_max=300)
+    d = inputs.make(wl)
+    g = _dev(d)
+    y = dsc.dsc_lowrank_fwd(g["x"], g["z"], g["U"], g["bias"], cu_seqlens=g["cu_seqlens"])
+    assert dsc.dsc_sync_status() == dsc.DSC_OK
+    ry = oracle_mod.lowrank_fwd(d["x"], d["z"], d["U"], d["bias"], W, cu_seqlens=d["cu_seqlens"])
+    assert_close(y.reshape(B * T, D), ry, "bf16", "y")
+
+
 def test_lowrank_fwd_deterministic(dsc):
     wl = inputs.custom(2, 300, 512, 4, R=64, dtype="bf16", seed_id=470, packed=True, doc_min=3, doc_max=50)
     g = _dev(inputs.make(wl))
@@ -137,6 +153,12 @@ def test_lowrank_bwd_full_size_sampled(dsc, oracle_mod):
     dx, dz, dU, db = _bwd_check(dsc, oracle_mod, wl, rows=rows, cols=cols)
     for t in (dx, dz, dU, db):
         assert torch.isfinite(t).all()
+
+
+def test_lowrank_bwd_runs_across_blocks(dsc, oracle_mod):
+    B, T, D, W, R = MULTI_RUN
+    wl = inputs.custom(B, T, D, W, R=R, dtype="bf16", seed_id=781, packed=True, doc_min=1, doc_max=300)
+    _bwd_check(dsc, oracle_mod, wl)
 
 
 def test_lowrank_bwd_deterministic_dx_and_close_repeat(dsc):
