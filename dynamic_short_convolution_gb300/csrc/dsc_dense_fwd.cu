@@ -38,6 +38,10 @@ __global__ void __launch_bounds__(32 * (1 + TileCfg<E, HPT, false>::NCW), 1)
         fence_mbarrier_init();
     }
     __syncthreads();
+    // this launch may overlap the end of the stream's previous kernel: every access to global memory
+    // comes after the wait; the next kernel may begin its own prologue as soon as this one runs
+    grid_dependents_launch();
+    grid_dependency_wait();
     volatile int *abort_flag = &hdr->abort_flag;
 
     if (warp == 0) {
@@ -194,8 +198,7 @@ static dsc_status launch_fwd_tma(const DenseArgs &a, const DeviceInfo &dev)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes);
     if (e != cudaSuccess) return DSC_ERR_CUDA;
     const DenseParams q = dense_params(a, plan, a.y, nullptr);
-    kern<<<plan.grid, plan.threads, plan.smem_bytes, a.stream>>>(tm_x, tm_w, q);
-    return launched();
+    return launch_overlapped(kern, plan.grid, plan.threads, plan.smem_bytes, a.stream, tm_x, tm_w, q);
 }
 
 template <typename E, int W>

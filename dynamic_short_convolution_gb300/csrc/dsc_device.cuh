@@ -136,6 +136,12 @@ __device__ __forceinline__ void tma_store_wait_all()
 // Make generic-proxy writes to shared memory visible to the async proxy (TMA, tcgen05).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch.  grid_dependency_wait(): wait until the grids this one was allowed to
+// overlap have completed and their memory operations are visible (returns at once when there are none).
+// grid_dependents_launch(): let the grids that may overlap this one begin launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ element groups
 
 template <typename E>

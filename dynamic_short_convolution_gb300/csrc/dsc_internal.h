@@ -79,6 +79,31 @@ inline dsc_status launched(unsigned n = 1)
     return cuda_status(e);
 }
 
+// Launch a kernel that may begin while the stream's previous kernel is still running (programmatic
+// dependent launch).  The kernel itself orders every access that depends on that previous kernel behind
+// grid_dependency_wait(); the previous kernel lets it start with grid_dependents_launch() or by exiting.
+template <typename... KArgs, typename... Args>
+inline dsc_status launch_overlapped(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                                    cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DSC_ERR_CUDA;
+    }
+    return launched();
+}
+
 inline unsigned align_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<unsigned long long>(p) & 15ull) == 0; }

@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
             int gcount = 0;  // groups processed (edge-buffer parity), equal across one column warp's quadrants
             bool epi_abort = false;
+            // the accumulation targets are zeroed by the kernel launched just before this one, which this
+            // kernel may overlap: every reduction into them comes after this wait
+            if (u == u_begin) grid_dependency_wait();
             DocCursor cursor;  // this thread's token increases from tile to tile within a run
             for (int v = 0; v < ntiles && !epi_abort; ++v) {
                 const int i = it + v;
@@ -651,7 +654,8 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
         if (*abort_flag) break;
     }
 
-    // ---- teardown: nothing of this CTA may still be in flight
+    // ---- teardown: nothing of this CTA may still be in flight; the dz cast kernel may start launching
+    grid_dependents_launch();
     if (warp == 0 && lane == 0) {
         if (*abort_flag)
             for (int s = 0; s < kStages; ++s)
@@ -668,6 +672,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
 // Zero the fp32 accumulation targets (the dz workspace, dU, db).
 __global__ void lowrank_bwd_zero(float4 *a, long long na4, float4 *b, long long nb4, float *c, int nc)
 {
+    grid_dependents_launch();  // the backward kernel may start its loads and MMAs now
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long i0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -679,6 +684,8 @@ __global__ void lowrank_bwd_zero(float4 *a, long long na4, float4 *b, long long 
 // dz = bf16(dz workspace), 8 elements per thread.
 __global__ void lowrank_bwd_cast(const float4 *src, uint4 *dst, long long n8)
 {
+    grid_dependents_launch();  // the next kernel may begin its prologue
+    grid_dependency_wait();    // every partial sum of the backward kernel is in
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
         const float4 a = src[2 * i], b = src[2 * i + 1];
@@ -769,12 +776,10 @@ static dsc_status launch_lowrank_bwd(const LowrankArgs &a, const DeviceInfo &dev
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return DSC_ERR_CUDA;
     const int grid = dev.sm_count < p.n_units ? dev.sm_count : p.n_units;
-    kern<<<grid, kThreads, smem, a.stream>>>(tm_z, tm_x, tm_dy, tm_u, tm_dx, p);
-    s = launched();
+    s = launch_overlapped(kern, grid, kThreads, smem, a.stream, tm_z, tm_x, tm_dy, tm_u, tm_dx, p);
     if (s != DSC_OK) return s;
-    lowrank_bwd_cast<<<dev.sm_count * 4, 256, 0, a.stream>>>(reinterpret_cast<const float4 *>(p.dz_ws),
-                                                             static_cast<uint4 *>(a.dz), nz / 8);
-    return launched();
+    return launch_overlapped(lowrank_bwd_cast, dev.sm_count * 4, 256, 0, a.stream,
+                             reinterpret_cast<const float4 *>(p.dz_ws), static_cast<uint4 *>(a.dz), nz / 8);
 }
 
 dsc_status lowrank_bwd(const LowrankArgs &a)

@@ -123,6 +123,10 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // this launch may overlap the end of the stream's previous kernel: every access to global memory
+    // comes after the wait; the next kernel may begin its own prologue as soon as this one runs
+    grid_dependents_launch();
+    grid_dependency_wait();
     const uint32_t tmem = hdr->tmem_base;
     volatile int *abort_flag = &hdr->abort_flag;
 
@@ -445,8 +449,7 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return DSC_ERR_CUDA;
     int grid = dev.sm_count < p.n_units ? dev.sm_count : p.n_units;
-    kern<<<grid, kThreads, smem, a.stream>>>(tm_z, tm_x, tm_y, tm_u, p);
-    return launched();
+    return launch_overlapped(kern, grid, kThreads, smem, a.stream, tm_z, tm_x, tm_y, tm_u, p);
 }
 
 dsc_status lowrank_fwd(const LowrankArgs &a)
