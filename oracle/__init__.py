@@ -15,6 +15,9 @@ section "Key design 1"):
 * ``bwd``:         dx, dw of <dy, y>                                    (derivative of eq. 2 + 3)
 * ``lowrank_fwd``: the same with w[t, d, k] = (z U + b)[t, d*W + k]     ("low-rank parameterization")
 * ``lowrank_bwd``: dx, dz, dU, db of <dy, y> for the low-rank form
+* ``static_fwd``:  y = x + sum_k w[d, k] * x~[t-k, d]                  (eq. 1 with the residual of eq. 3)
+* ``static_bwd``:  dx rows and dw [D, W] (summed over every token) of <dy, y>
+* ``decode_step``: y of one new token per sequence against a history ring (eq. 2 + eq. 3, one step)
 
 Every function takes tensors laid out exactly like the CUDA library's
 arguments: x, y, dy, dx ``[B, T, D]``; head-wise / materialised w
@@ -72,6 +75,9 @@ def _load():
             lib.dsco_lowrank_bwd_rows.argtypes = [vp, vp, vp, vp, i32, vp, i32, i64, i64, i32, i64, vp, i64, i64,
                                                   vp, vp]
             lib.dsco_lowrank_bwd_params.argtypes = [vp, vp, vp, i32, i64, i64, i32, i64, vp, vp, i64, vp, vp]
+            lib.dsco_static_fwd_rows.argtypes = [vp, vp, i32, i64, i64, i32, vp, i64, i64, vp]
+            lib.dsco_static_bwd.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i64, i64, vp, vp]
+            lib.dsco_decode_step.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i64, vp]
             _lib = lib
     return _lib
 
@@ -226,3 +232,54 @@ def lowrank_bwd(x, z, U, bias, dy, W: int, cu_seqlens=None, rows=None, cols=None
             out["db"] = db
     del kx, kz, ku, kg, kb
     return out
+
+
+def static_fwd(x, w, W: int, cu_seqlens=None, rows=None) -> np.ndarray:
+    """Static filter w [D, W]: y rows [r0, r1) as float64 [r1-r0, D]."""
+    B, T, D = x.shape
+    BT = B * T
+    assert tuple(w.shape) == (D, W)
+    px, cx, kx = _raw(x)
+    pw, cw, kw = _raw(w)
+    dt = _same_dtype(cx, cw)
+    ds = docstarts(B, T, cu_seqlens)
+    r0, r1 = _rows(rows, BT)
+    y = np.empty((r1 - r0, D), dtype=np.float64)
+    _load().dsco_static_fwd_rows(px, pw, dt, BT, D, W, _ptr(ds), r0, r1, _ptr(y))
+    del kx, kw
+    return y
+
+
+def static_bwd(x, w, dy, W: int, cu_seqlens=None, rows=None, want_dx=True, want_dw=True):
+    """(dx rows [r1-r0, D], dw [D, W] summed over every token) as float64 (None where not wanted)."""
+    B, T, D = x.shape
+    BT = B * T
+    assert tuple(w.shape) == (D, W) and tuple(dy.shape) == (B, T, D)
+    px, cx, kx = _raw(x)
+    pw, cw, kw = _raw(w)
+    pg, cg, kg = _raw(dy)
+    dt = _same_dtype(cx, cw, cg)
+    ds = docstarts(B, T, cu_seqlens)
+    r0, r1 = _rows(rows, BT)
+    dx = np.empty((r1 - r0, D), dtype=np.float64) if want_dx else None
+    dw = np.empty((D, W), dtype=np.float64) if want_dw else None
+    _load().dsco_static_bwd(px, pw, pg, dt, BT, D, W, _ptr(ds), r0, r1, _ptr(dx), _ptr(dw))
+    del kx, kw, kg
+    return dx, dw
+
+
+def decode_step(x, w, hist, pos, W: int, H: int) -> np.ndarray:
+    """One decode step: x [B, D], w [B, D/H, W], hist [B, W-1, D] (ring: slot p mod (W-1) holds the input
+    at document position p), pos [B] int (this token's position in its document).  Returns y [B, D] float64."""
+    B, D = x.shape
+    assert D % H == 0 and tuple(w.shape) == (B, D // H, W) and tuple(hist.shape) == (B, max(W - 1, 0), D)
+    px, cx, kx = _raw(x)
+    pw, cw, kw = _raw(w)
+    ph, ch, kh = _raw(hist)
+    dt = _same_dtype(cx, cw, ch)
+    pz = np.ascontiguousarray(np.asarray(pos.cpu() if isinstance(pos, torch.Tensor) else pos, dtype=np.int32))
+    assert pz.shape == (B,) and (pz >= 0).all()
+    y = np.empty((B, D), dtype=np.float64)
+    _load().dsco_decode_step(px, pw, ph, _ptr(pz), dt, B, D, W, H, _ptr(y))
+    del kx, kw, kh
+    return y

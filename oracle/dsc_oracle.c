@@ -31,6 +31,10 @@
  *     dz[t,r] = sum_n G[t,n] U[r,n],  dU[r,n] = sum_t z[t,r] G[t,n],
  *     db[n]   = sum_t G[t,n].
  *
+ *   Also: the static form (eq. 1, one filter w[d,k] for all tokens) with the
+ *   same residual and masking, its backward (dw summed over every token), and
+ *   one decode step of eq. 2 + 3 against a per-sequence history ring.
+ *
  * Tokens are indexed on the flattened B*T axis; docstart(t) >= (t / T) * T
  * always, so sequences never see each other.  Every product and sum is done
  * in IEEE double from inputs converted exactly (fp32, bf16 or fp64 storage).
@@ -238,6 +242,92 @@ void dsco_lowrank_bwd_params(const void *x, const void *z, const void *dy, int d
                     acc += load(z, dt, t * R + r) * gfil(x, dy, dt, D, W, ds, t, n);
                 dU[r * ncols + i] = acc;
             }
+        }
+    }
+}
+
+/*
+ * Static short convolution (eq. 1: one filter w[d][k] for every token), with the residual placement of
+ * eq. 3 and the same zero history before each document start:
+ *   y[t,d] = x[t,d] + sum_{k<W} w[d,k] * xt(t, t-k, d)
+ * rows [r0, r1); w is [D, W].
+ */
+void dsco_static_fwd_rows(const void *x, const void *w, int dt, int64_t BT, int64_t D, int W, const int64_t *ds,
+                          int64_t r0, int64_t r1, double *y)
+{
+    (void)BT;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = r0; t < r1; ++t) {
+        for (int64_t d = 0; d < D; ++d) {
+            double acc = load(x, dt, t * D + d);
+            for (int k = 0; k < W; ++k)
+                acc += load(w, dt, d * W + k) * xt(x, dt, D, ds, t, t - k, d);
+            y[(t - r0) * D + d] = acc;
+        }
+    }
+}
+
+/*
+ * Static backward.  dx rows [r0, r1) (dx may be NULL):
+ *   dx[s,d] = dy[s,d] + sum_{k<W, s+k<BT, s>=docstart(s+k)} w[d,k] dy[s+k,d]
+ * dw [D, W] over every token of the flattened axis (dw may be NULL):
+ *   dw[d,k] = sum_t dy[t,d] * xt(t, t-k, d)
+ */
+void dsco_static_bwd(const void *x, const void *w, const void *dy, int dt, int64_t BT, int64_t D, int W,
+                     const int64_t *ds, int64_t r0, int64_t r1, double *dx, double *dw)
+{
+    if (dx) {
+#pragma omp parallel for schedule(static)
+        for (int64_t s = r0; s < r1; ++s) {
+            for (int64_t d = 0; d < D; ++d) {
+                double acc = load(dy, dt, s * D + d);
+                for (int k = 0; k < W; ++k) {
+                    int64_t t = s + k;
+                    if (t < BT && s >= ds[t])
+                        acc += load(w, dt, d * W + k) * load(dy, dt, t * D + d);
+                }
+                dx[(s - r0) * D + d] = acc;
+            }
+        }
+    }
+    if (dw) {
+#pragma omp parallel for schedule(static)
+        for (int64_t d = 0; d < D; ++d) {
+            for (int k = 0; k < W; ++k) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < BT; ++t)
+                    acc += load(dy, dt, t * D + d) * xt(x, dt, D, ds, t, t - k, d);
+                dw[d * W + k] = acc;
+            }
+        }
+    }
+}
+
+/*
+ * One decode step of eq. 2 + eq. 3 for B sequences, each at one new token.  x[b, D] is the token's
+ * input, w[b, D/H, W] its filter, pos[b] its position within its document, and hist[b, W-1, D] a ring
+ * whose slot (p mod (W-1)) holds the input of the document's token at position p:
+ *   y[b,d] = x[b,d] + w[b,g(d),0] x[b,d] + sum_{1<=k<W, k<=pos[b]} w[b,g(d),k] hist[b, (pos[b]-k) mod (W-1), d]
+ * (a history token before the document start contributes zero).  Only y is computed here; the ring
+ * update (slot pos[b] mod (W-1) := x[b]) is a copy.
+ */
+void dsco_decode_step(const void *x, const void *w, const void *hist, const int32_t *pos, int dt, int64_t B,
+                      int64_t D, int W, int64_t H, double *y)
+{
+    const int64_t G = D / H;
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t p = pos[b];
+        for (int64_t d = 0; d < D; ++d) {
+            const double xv = load(x, dt, b * D + d);
+            double acc = xv + load(w, dt, (b * G + d / H) * W + 0) * xv;
+            for (int k = 1; k < W; ++k) {
+                if (p - k < 0)
+                    continue;
+                const int64_t slot = (p - k) % (W - 1);
+                acc += load(w, dt, (b * G + d / H) * W + k) * load(hist, dt, (b * (W - 1) + slot) * D + d);
+            }
+            y[b * D + d] = acc;
         }
     }
 }
