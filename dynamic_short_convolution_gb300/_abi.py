@@ -36,6 +36,9 @@ SIGNATURES = {
                              _vp]),
     "dsc_lowrank_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i,
                                      _vp]),
+    "dsc_static_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "dsc_static_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "dsc_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "dsc_validate_cu_seqlens": (_i, [_vp, _i, _i, _i, _vp]),
     "dsc_sync_status": (_i, [_vp]),
     "dsc_test_wait_timeout": (_i, [_u64, _vp]),
@@ -202,6 +205,52 @@ def dsc_lowrank_bwd_noalloc(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=Non
                                       _dt(x), cu, n, _stream(stream))
     _check(s, "dsc_lowrank_bwd_noalloc")
     return dx, dz, dU, db
+
+
+def dsc_static_fwd(x, w, y=None, *, cu_seqlens=None, stream=None):
+    """Static short convolution: x [B,T,D], w [D,W] (one filter for every token); returns y [B,T,D]."""
+    B, T, D = x.shape
+    if w.dim() != 2 or w.shape[0] != D:
+        raise ValueError("shapes: x [B,T,D]; w [D,W]")
+    W = w.shape[1]
+    y = torch.empty_like(x) if y is None else y
+    cu, n = _cu(cu_seqlens)
+    s = lib().dsc_static_fwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(y, "y", x.dtype), B, T, D, W, _dt(x), cu, n,
+                             _stream(stream))
+    _check(s, "dsc_static_fwd")
+    return y
+
+
+def dsc_static_bwd(x, w, dy, dx=None, dw=None, *, cu_seqlens=None, stream=None):
+    """(dx [B,T,D], dw [D,W] fp32) of the static convolution for the upstream gradient dy."""
+    B, T, D = x.shape
+    if w.dim() != 2 or w.shape[0] != D or tuple(dy.shape) != (B, T, D):
+        raise ValueError("shapes: x, dy [B,T,D]; w [D,W]")
+    W = w.shape[1]
+    dx = torch.empty_like(x) if dx is None else dx
+    dw = torch.empty((D, W), dtype=torch.float32, device=x.device) if dw is None else dw
+    cu, n = _cu(cu_seqlens)
+    s = lib().dsc_static_bwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(dy, "dy", x.dtype), _dev(dx, "dx", x.dtype),
+                             _dev(dw, "dw", torch.float32), B, T, D, W, _dt(x), cu, n, _stream(stream))
+    _check(s, "dsc_static_bwd")
+    return dx, dw
+
+
+def dsc_decode_step(x, w, hist, pos, y=None, *, stream=None):
+    """One decode step for B sequences: x [B,D], w [B,D/H,W], hist [B,W-1,D] (ring, updated in place),
+    pos [B] int32 (document positions, read only); returns y [B,D]."""
+    B, D = x.shape
+    if w.dim() != 3 or w.shape[0] != B or w.shape[1] < 1 or D % w.shape[1]:
+        raise ValueError("shapes: x [B,D]; w [B,D/H,W]")
+    W = w.shape[2]
+    if tuple(hist.shape) != (B, W - 1, D) or tuple(pos.shape) != (B,):
+        raise ValueError("shapes: hist [B,W-1,D]; pos [B]")
+    y = torch.empty_like(x) if y is None else y
+    hp = _dev(hist, "hist", x.dtype) if W > 1 else None
+    s = lib().dsc_decode_step(_dev(x, "x"), _dev(w, "w", x.dtype), hp, _dev(pos, "pos", torch.int32),
+                              _dev(y, "y", x.dtype), B, D, W, D // w.shape[1], _dt(x), _stream(stream))
+    _check(s, "dsc_decode_step")
+    return y
 
 
 def dsc_validate_cu_seqlens(cu_seqlens, B, T, *, stream=None) -> None:

@@ -241,6 +241,52 @@ dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const fl
     return lowrank_bwd(a);
 }
 
+dsc_status dsc_static_fwd(const void *x, const void *w, void *y, int B, int T, int D, int W, dsc_dtype dt,
+                          const int32_t *cu_seqlens, int n_docs, cudaStream_t stream)
+{
+    if (dt != DSC_F32 && dt != DSC_BF16) return DSC_ERR_INVALID_ARG;
+    const int es = dt == DSC_BF16 ? 2 : 4;
+    if (!dims_ok(B, T, D, W) || !cu_ok(cu_seqlens, n_docs)) return DSC_ERR_INVALID_ARG;
+    if (!elem_aligned(x, es) || !elem_aligned(w, es) || !elem_aligned(y, es)) return DSC_ERR_INVALID_ARG;
+    StaticArgs a;
+    a.x = x; a.w = w; a.y = y;
+    a.B = B; a.T = T; a.D = D; a.W = W; a.dt = dt;
+    a.cu = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0; a.stream = stream;
+    return static_fwd(a);
+}
+
+dsc_status dsc_static_bwd(const void *x, const void *w, const void *dy, void *dx, float *dw, int B, int T, int D,
+                          int W, dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream)
+{
+    if (dt != DSC_F32 && dt != DSC_BF16) return DSC_ERR_INVALID_ARG;
+    const int es = dt == DSC_BF16 ? 2 : 4;
+    if (!dims_ok(B, T, D, W) || !cu_ok(cu_seqlens, n_docs)) return DSC_ERR_INVALID_ARG;
+    if (!elem_aligned(x, es) || !elem_aligned(w, es) || !elem_aligned(dy, es) || !elem_aligned(dx, es) ||
+        !elem_aligned(dw, 4))
+        return DSC_ERR_INVALID_ARG;
+    StaticArgs a;
+    a.x = x; a.w = w; a.dy = dy; a.dx = dx; a.dw = dw;
+    a.B = B; a.T = T; a.D = D; a.W = W; a.dt = dt;
+    a.cu = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0; a.stream = stream;
+    return static_bwd(a);
+}
+
+dsc_status dsc_decode_step(const void *x, const void *w, void *hist, const int32_t *pos, void *y, int B, int D, int W,
+                           int H, dsc_dtype dt, cudaStream_t stream)
+{
+    if (dt != DSC_F32 && dt != DSC_BF16) return DSC_ERR_INVALID_ARG;
+    const int es = dt == DSC_BF16 ? 2 : 4;
+    if (!dims_ok(B, 1, D, W) || H < 1 || D % H != 0) return DSC_ERR_INVALID_ARG;
+    if (!elem_aligned(x, es) || !elem_aligned(w, es) || !elem_aligned(y, es) || !elem_aligned(pos, 4))
+        return DSC_ERR_INVALID_ARG;
+    if (W > 1 && !elem_aligned(hist, es)) return DSC_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * (W - 1) * D >= (1LL << 31)) return DSC_ERR_INVALID_ARG;
+    DecodeArgs a;
+    a.x = x; a.w = w; a.hist = hist; a.pos = pos; a.y = y;
+    a.B = B; a.D = D; a.W = W; a.H = H; a.dt = dt; a.stream = stream;
+    return decode_step(a);
+}
+
 dsc_status dsc_validate_cu_seqlens(const int32_t *cu_seqlens, int n_docs, int B, int T, cudaStream_t stream)
 {
     if (!cu_seqlens || n_docs < 1 || B < 1 || T < 1) return DSC_ERR_INVALID_ARG;

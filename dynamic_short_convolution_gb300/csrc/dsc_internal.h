@@ -42,11 +42,41 @@ struct LowrankArgs {
     cudaStream_t stream = nullptr;
 };
 
+// Arguments of the static short convolution (filter w [D, W]; dw fp32 [D, W]).
+struct StaticArgs {
+    const void *x = nullptr;
+    const void *w = nullptr;
+    const void *dy = nullptr;
+    void *y = nullptr;
+    void *dx = nullptr;
+    float *dw = nullptr;
+    int B = 0, T = 0, D = 0, W = 0;
+    dsc_dtype dt = DSC_BF16;
+    const int32_t *cu = nullptr;
+    int n_docs = 0;
+    cudaStream_t stream = nullptr;
+};
+
+// Arguments of one decode step (x, y [B, D]; w [B, D/H, W]; hist [B, W-1, D]; pos [B]).
+struct DecodeArgs {
+    const void *x = nullptr;
+    const void *w = nullptr;
+    void *hist = nullptr;
+    const int32_t *pos = nullptr;
+    void *y = nullptr;
+    int B = 0, D = 0, W = 0, H = 0;
+    dsc_dtype dt = DSC_BF16;
+    cudaStream_t stream = nullptr;
+};
+
 dsc_status dense_fwd(const DenseArgs &a);
 dsc_status dense_bwd(const DenseArgs &a);
 dsc_status lowrank_fwd(const LowrankArgs &a);
 dsc_status lowrank_bwd(const LowrankArgs &a);
 size_t lowrank_bwd_workspace(int B, int T, int D, int W, int R);
+dsc_status static_fwd(const StaticArgs &a);
+dsc_status static_bwd(const StaticArgs &a);
+dsc_status decode_step(const DecodeArgs &a);
 
 // Per-device status word (device address) and the current wait limit.
 int *device_status_word();

@@ -17,11 +17,18 @@ for real activations):
 * ``qkv_packed_bf16`` B=4 T=8192 D=3072 W=4 H=16 bf16 over packed documents with
   lengths ~U{128..4096} per sequence (the last one truncated to fill T);
   w~N(0,0.1)
+* ``static_bf16``   B=8 T=2048 D=2048 W=4 bf16, one filter w [D, W] for every token
+  (eq. 1), w = 0.1*N(0,1) + 0.5 on tap k=0: the head-wise workload's shape and
+  filter statistics, so the static and dynamic kernels can be compared
+* ``decode_bf16``   B=512 sequences, one new token each, D=6144 (Q, K and V of a
+  2048-wide model side by side), W=4 H=16 bf16; history ring [B, W-1, D] ~N(0,1),
+  positions ~U{0..4095} (a fifth of them below W-1, where the document's history
+  is shorter than the filter)
 
 Upstream gradients dy ~ N(0,1) everywhere.  N(0, s) means variance s.
 Values are drawn in fp32 and rounded to nearest-even bf16 where the workload
 is bf16.  Seeds: 1000 * workload id + tensor index (x=0, w=1, dy=2, z=3, U=4,
-bias=5, document lengths=6).
+bias=5, document lengths=6, decode history=7, decode positions=8).
 """
 from __future__ import annotations
 
@@ -30,14 +37,14 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-X, WGT, DY, Z, U, BIAS, LENS = range(7)
+X, WGT, DY, Z, U, BIAS, LENS, HIST, POS = range(9)
 
 
 @dataclass(frozen=True)
 class Workload:
     wid: int
     name: str
-    kind: str            # "dense" (materialised / head-wise) or "lowrank"
+    kind: str            # "dense" (materialised / head-wise), "lowrank", "static" or "decode"
     B: int
     T: int
     D: int
@@ -67,6 +74,8 @@ WORKLOADS = {
     3: Workload(3, "material_bf16", "dense", 4, 4096, 2048, 4, H=1, w_std=math.sqrt(0.1)),
     4: Workload(4, "lowrank_bf16", "lowrank", 8, 2048, 2048, 4, R=64),
     5: Workload(5, "qkv_packed_bf16", "dense", 4, 8192, 3072, 4, H=16, w_std=math.sqrt(0.1), packed=True),
+    6: Workload(6, "static_bf16", "static", 8, 2048, 2048, 4, w_std=0.1, w_tap0=0.5),
+    7: Workload(7, "decode_bf16", "decode", 512, 1, 6144, 4, H=16, w_std=0.1, w_tap0=0.5, extra={"max_pos": 4096}),
 }
 
 
@@ -118,8 +127,16 @@ def doc_offsets(wl: Workload) -> torch.Tensor | None:
 def make(wl: Workload, with_grad: bool = True) -> dict:
     """All inputs of one workload as CPU tensors."""
     dt = wl.torch_dtype
+    if wl.kind == "decode":
+        return make_decode(wl)
     out = {"x": _normal((wl.B, wl.T, wl.D), 1.0, wl.wid, X, dt)}
-    if wl.kind == "dense":
+    if wl.kind == "static":
+        w = torch.randn(wl.D, wl.W, generator=_gen(wl.wid, WGT), dtype=torch.float32)
+        w.mul_(wl.w_std)
+        if wl.w_tap0:
+            w[:, 0] += wl.w_tap0
+        out["w"] = w.to(dt)
+    elif wl.kind == "dense":
         w = torch.randn(wl.B, wl.T, wl.D // wl.H, wl.W, generator=_gen(wl.wid, WGT), dtype=torch.float32)
         w.mul_(wl.w_std)
         if wl.w_tap0:
@@ -133,6 +150,38 @@ def make(wl: Workload, with_grad: bool = True) -> dict:
         out["dy"] = _normal((wl.B, wl.T, wl.D), 1.0, wl.wid, DY, dt)
     out["cu_seqlens"] = doc_offsets(wl)
     return out
+
+
+def make_decode(wl: Workload) -> dict:
+    """One decode step's inputs: x [B, D], w [B, D/H, W], hist [B, W-1, D] (a ring of past inputs),
+    pos [B] int32 (each token's position in its document; about a fifth below W-1)."""
+    dt = wl.torch_dtype
+    out = {"x": _normal((wl.B, wl.D), 1.0, wl.wid, X, dt)}
+    w = torch.randn(wl.B, wl.D // wl.H, wl.W, generator=_gen(wl.wid, WGT), dtype=torch.float32)
+    w.mul_(wl.w_std)
+    if wl.w_tap0:
+        w[..., 0] += wl.w_tap0
+    out["w"] = w.to(dt)
+    out["hist"] = _normal((wl.B, wl.W - 1, wl.D), 1.0, wl.wid, HIST, dt)
+    g = _gen(wl.wid, POS)
+    max_pos = int(wl.extra.get("max_pos", 4096))
+    pos = torch.randint(0, max_pos, (wl.B,), generator=g, dtype=torch.int64)
+    short = torch.rand(wl.B, generator=g) < 0.2
+    pos = torch.where(short, torch.randint(0, max(wl.W - 1, 1), (wl.B,), generator=g, dtype=torch.int64), pos)
+    out["pos"] = pos.to(torch.int32)
+    return out
+
+
+def custom_decode(B, D, W, H=1, dtype="bf16", seed_id=200, w_std=0.5, max_pos=64) -> Workload:
+    """A decode workload of arbitrary shape for tests (seeded by ``seed_id``)."""
+    return Workload(seed_id, "custom_decode", "decode", B, 1, D, W, H=H, dtype=dtype, w_std=w_std,
+                    extra={"max_pos": max_pos})
+
+
+def custom_static(B, T, D, W, dtype="bf16", seed_id=300, w_std=0.5, packed=False, doc_min=1, doc_max=None) -> Workload:
+    """A static-filter workload of arbitrary shape for tests (seeded by ``seed_id``)."""
+    return Workload(seed_id, "custom_static", "static", B, T, D, W, dtype=dtype, w_std=w_std, packed=packed,
+                    doc_min=doc_min, doc_max=doc_max if doc_max is not None else T)
 
 
 def shrink(wl: Workload, T: int) -> Workload:

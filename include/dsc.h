@@ -164,6 +164,55 @@ dsc_status dsc_lowrank_bwd_noalloc(const void *x, const void *z, const void *U, 
                                    dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
 
 /*
+ * dsc_static_fwd -- the static short convolution: one filter for every token
+ *   ("Parameterization", eq. 1), applied with the residual of eq. 3 and the
+ *   same zero history before sequence and document starts:
+ *     y[t,d] = x[t,d] + sum_{k<W} w[d,k] * x~[t-k, d]
+ *   x [B,T,D] and w [D,W] (tap k innermost) in dtype dt; writes y [B,T,D].
+ *   Requirements as dsc_fwd (no H).  The fast path wants D % 8 == 0 and
+ *   16-byte aligned pointers; other shapes take a slower element-wise path.
+ */
+dsc_status dsc_static_fwd(const void *x, const void *w, void *y, int B, int T, int D, int W, dsc_dtype dt,
+                          const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
+
+/*
+ * dsc_static_bwd -- backward pass of dsc_static_fwd for an upstream gradient dy:
+ *     dx[s,d] = dy[s,d] + sum_{k<W, s+k in s's document} w[d,k] dy[s+k, d]
+ *     dw[d,k] = sum over every token t of dy[t,d] * x~[t-k, d]
+ *   x, w, dy in dtype dt; writes dx [B,T,D] (dtype dt) and dw [D,W] in fp32
+ *   (both overwritten).  dw is summed with fp32 atomic additions, so the
+ *   order of its additions, and its last bits, may vary from call to call.
+ *   Requirements as dsc_static_fwd.
+ */
+dsc_status dsc_static_bwd(const void *x, const void *w, const void *dy, void *dx, float *dw, int B, int T, int D,
+                          int W, dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
+
+/*
+ * dsc_decode_step -- one inference step of eq. 2 + eq. 3 for B sequences, one
+ *   new token each, against a per-sequence history of the last W-1 inputs.
+ *   The notes list inference optimisation as open work ("Discussion and
+ *   limitations"); this is the single-token form of dsc_fwd.
+ *     x [B,D]        this step's inputs (dtype dt)
+ *     w [B,D/H,W]    their filters (head size H as in dsc_fwd)
+ *     pos [B] int32  the position of each token within its document
+ *                    (0 = the document's first token); read only -- the
+ *                    caller advances it
+ *     hist [B,W-1,D] a ring of past inputs: slot (p mod (W-1)) holds the input
+ *                    of the document's token at position p.  Read, then the
+ *                    slot (pos mod (W-1)) is overwritten with x (W > 1; with
+ *                    W == 1 hist is not touched and may be NULL)
+ *     y [B,D]        y[b,d] = x[b,d] + sum_{k<W, k<=pos[b]} w[b,g(d),k] * x_{pos-k}
+ *   History before a document start is zero because pos says where the
+ *   document starts, so a new document needs no reset of hist.  A negative
+ *   pos is treated as 0 and recorded as DSC_ERR_INVALID_ARG in the device
+ *   status word.  Requirements: B, D >= 1; 1 <= W <= 8; D % H == 0;
+ *   B*(W-1)*D < 2^31.  The fast path wants (16 / element size) | D and x, y,
+ *   hist 16-byte aligned.
+ */
+dsc_status dsc_decode_step(const void *x, const void *w, void *hist, const int32_t *pos, void *y, int B, int D, int W,
+                           int H, dsc_dtype dt, cudaStream_t stream);
+
+/*
  * dsc_validate_cu_seqlens -- device-side check of packed-document offsets:
  * cu[0] == 0, strictly increasing, cu[n_docs] == B*T.  Asynchronous; a
  * violation is recorded as DSC_ERR_INVALID_ARG in the device status word,

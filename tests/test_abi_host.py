@@ -28,7 +28,7 @@ def _declared():
 def test_header_declares_the_abi():
     names = _declared()
     for n in ("dsc_fwd", "dsc_bwd", "dsc_lowrank_fwd", "dsc_lowrank_bwd", "dsc_lowrank_bwd_workspace_bytes",
-              "dsc_status_string", "dsc_sync_status"):
+              "dsc_static_fwd", "dsc_static_bwd", "dsc_decode_step", "dsc_status_string", "dsc_sync_status"):
         assert n in names
 
 
@@ -69,6 +69,19 @@ def test_rejects_bad_arguments_before_any_launch(L):
         assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, p, 1, 8, 64, 4, r, bf16, None, 0, None) == 2
     assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, 16, bf16, None, 0, None) == 1  # no workspace
     assert L.dsc_validate_cu_seqlens(None, 3, 1, 8, None) == 1
+    # static convolution: the same size, W, dtype and alignment rules; dw must be fp32-aligned
+    assert L.dsc_static_fwd(p, p, p, 0, 8, 64, 4, bf16, None, 0, None) == 1
+    assert L.dsc_static_fwd(p, p, p, 1, 8, 64, 9, bf16, None, 0, None) == 1
+    assert L.dsc_static_fwd(p, p, p, 1, 8, 64, 4, 7, None, 0, None) == 1
+    assert L.dsc_static_fwd(p, p, p, 1, 8, 64, 4, bf16, p, 0, None) == 1
+    assert L.dsc_static_bwd(p, p, p, p, ctypes.c_void_p(0x10002), 1, 8, 64, 4, bf16, None, 0, None) == 1
+    assert L.dsc_static_bwd(p, p, p, None, p, 1, 8, 64, 4, bf16, None, 0, None) == 1
+    # decode step: D % H, W range, missing history for W > 1, missing positions
+    assert L.dsc_decode_step(p, p, p, p, p, 4, 64, 4, 3, bf16, None) == 1
+    assert L.dsc_decode_step(p, p, p, p, p, 4, 64, 9, 1, bf16, None) == 1
+    assert L.dsc_decode_step(p, p, None, p, p, 4, 64, 4, 1, bf16, None) == 1
+    assert L.dsc_decode_step(p, p, p, None, p, 4, 64, 4, 1, bf16, None) == 1
+    assert L.dsc_decode_step(p, p, p, p, p, 0, 64, 4, 1, bf16, None) == 1
 
 
 def test_loading_without_gpu_reports_cuda_error_not_crash(L):
