@@ -75,10 +75,12 @@ DENSE_BWD_SRC = ["dsc_dense_bwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 DENSE_FWD_SRC = ["dsc_dense_fwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 LOWRANK_BWD_SRC = ["dsc_lowrank_bwd.cu", "dsc_tcgen05.cuh", "dsc_device.cuh"]
 LOWRANK_FWD_SRC = ["dsc_lowrank_fwd.cu", "dsc_tcgen05.cuh", "dsc_device.cuh"]
+STATIC_SRC = ["dsc_static.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 # (kernel name in the ncu launch list, source files) per workload kind and direction
 KERNELS = {("dense", "bwd"): ("dense_bwd_tma", DENSE_BWD_SRC), ("dense", "fwd"): ("dense_fwd_tma", DENSE_FWD_SRC),
            ("lowrank", "bwd"): ("lowrank_bwd_tc", LOWRANK_BWD_SRC),
-           ("lowrank", "fwd"): ("lowrank_fwd_tc", LOWRANK_FWD_SRC)}
+           ("lowrank", "fwd"): ("lowrank_fwd_tc", LOWRANK_FWD_SRC),
+           ("static", "bwd"): ("static_bwd_tma", STATIC_SRC), ("static", "fwd"): ("static_fwd_tma", STATIC_SRC)}
 
 
 def measured_traffic(kernel, workload, digest):
@@ -273,8 +275,113 @@ class LowrankProblem:
                             c["ws"], cu_seqlens=c["cu"])
 
 
+class StaticProblem:
+    """The static short convolution: one filter w [D, W] for every token; dw fp32 [D, W]."""
+
+    def __init__(self, wl, dev):
+        import torch
+
+        from dynamic_short_convolution_gb300 import inputs
+
+        self.wl = wl
+        d = inputs.make(wl)
+        self.host = d
+        g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+        t = {"x": g["x"], "w": g["w"], "dy": g["dy"], "cu": g["cu_seqlens"], "y": torch.empty_like(g["x"]),
+             "dx": torch.empty_like(g["x"]), "dw": torch.empty((wl.D, wl.W), dtype=torch.float32, device=dev)}
+        xb = g["x"].numel() * g["x"].element_size()
+        wb = g["w"].numel() * g["w"].element_size()
+        cb = 0 if g["cu_seqlens"] is None else g["cu_seqlens"].numel() * 4
+        self.bytes_fwd = 2 * xb + wb + cb
+        self.bytes_bwd = 3 * xb + wb + 4 * wl.D * wl.W + cb
+        self.flops_fwd = self.flops_bwd = 0
+        self.rot = _Sets(t, 4 * xb)
+        self.cur = t
+
+    def __getattr__(self, name):
+        cur = self.__dict__.get("cur")
+        if cur is not None and name in cur:
+            return cur[name]
+        raise AttributeError(name)
+
+    def advance(self):
+        self.cur = self.rot.next()
+
+    def fwd(self):
+        import dynamic_short_convolution_gb300 as dsc
+
+        c = self.cur
+        dsc.dsc_static_fwd(c["x"], c["w"], c["y"], cu_seqlens=c["cu"])
+
+    def bwd(self):
+        import dynamic_short_convolution_gb300 as dsc
+
+        c = self.cur
+        dsc.dsc_static_bwd(c["x"], c["w"], c["dy"], c["dx"], c["dw"], cu_seqlens=c["cu"])
+
+
+class DecodeProblem:
+    """One decode step of B sequences (inference: no backward).  The algorithmic bytes count x, w, the
+    history rows each token's document actually has (min(pos, W-1) of them), y, and the one ring slot
+    written."""
+
+    def __init__(self, wl, dev):
+        import torch
+
+        from dynamic_short_convolution_gb300 import inputs
+
+        self.wl = wl
+        d = inputs.make(wl)
+        self.host = d
+        g = {k: v.to(dev) for k, v in d.items()}
+        t = {"x": g["x"], "w": g["w"], "hist": g["hist"], "pos": g["pos"], "y": torch.empty_like(g["x"])}
+        es = g["x"].element_size()
+        row = wl.D * es
+        hist_rows = int(torch.clamp(d["pos"].long(), max=wl.W - 1).sum())
+        self.bytes_fwd = (2 * wl.B * row + g["w"].numel() * es + hist_rows * row + (wl.B * row if wl.W > 1 else 0)
+                          + wl.B * 4)
+        self.bytes_bwd = 0
+        self.flops_fwd = self.flops_bwd = 0
+        self.rot = _Sets(t, 2 * wl.B * row + g["hist"].numel() * es)
+        self.cur = t
+
+    def __getattr__(self, name):
+        cur = self.__dict__.get("cur")
+        if cur is not None and name in cur:
+            return cur[name]
+        raise AttributeError(name)
+
+    def advance(self):
+        self.cur = self.rot.next()
+
+    def fwd(self):
+        import dynamic_short_convolution_gb300 as dsc
+
+        c = self.cur
+        dsc.dsc_decode_step(c["x"], c["w"], c["hist"], c["pos"], c["y"])
+
+    def bwd(self):
+        pass
+
+
 def make_problem(wl, dev):
-    return LowrankProblem(wl, dev) if wl.kind == "lowrank" else DenseProblem(wl, dev)
+    return {"lowrank": LowrankProblem, "static": StaticProblem, "decode": DecodeProblem}.get(wl.kind, DenseProblem)(wl, dev)
+
+
+def time_back_to_back(prob, steps):
+    """Device time per forward call (ms) for a kernel shorter than the host's launch path: a GPU sleep
+    lets the host queue every call first, then they run back to back between two events."""
+    import torch
+
+    torch.cuda._sleep(int(2e6) + steps * 60000)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        prob.advance()
+        prob.fwd()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
 
 
 def time_steps(prob, steps):
@@ -324,7 +431,10 @@ def oracle_tokens_per_s(wl, budget_s, min_tokens=64):
 
 
 def _oracle_step(oracle, wl, d, r0, r1):
-    if wl.kind == "lowrank":
+    if wl.kind == "static":
+        oracle.static_fwd(d["x"], d["w"], wl.W, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
+        oracle.static_bwd(d["x"], d["w"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"], rows=(r0, r1), want_dw=False)
+    elif wl.kind == "lowrank":
         oracle.lowrank_fwd(d["x"], d["z"], d["U"], d["bias"], wl.W, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
         oracle.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
                            rows=(r0, r1), want=("dx", "dz"))
@@ -414,6 +524,8 @@ def main():
     from dynamic_short_convolution_gb300 import inputs
 
     wl = inputs.by_name(args.workload)
+    if wl.kind == "decode":
+        raise SystemExit("the decode step has no backward pass: it is measured in the rows table only")
     if args.impl == "reference":
         return run_reference(args, wl, rank, world)
 
@@ -478,7 +590,7 @@ def main():
 
     # roofline of the dominant kernel: HBM bytes, or tensor-core flops where those take longer at peak
     direction = "bwd" if mean_b >= mean_f else "fwd"
-    kname, ksrc = KERNELS[("lowrank" if wl.kind == "lowrank" else "dense", direction)]
+    kname, ksrc = KERNELS[(wl.kind if wl.kind in ("lowrank", "static") else "dense", direction)]
     kms = mean_b if direction == "bwd" else mean_f
     kbytes = prob.bytes_bwd if direction == "bwd" else prob.bytes_fwd
     kflops = prob.flops_bwd if direction == "bwd" else prob.flops_fwd
@@ -601,6 +713,16 @@ def measure_rows(dev, hbm_peak, tc_peak):
                 prob.fwd()
                 prob.bwd()
             torch.cuda.synchronize()
+            if wl.kind == "decode":
+                ms = time_back_to_back(prob, 200)
+                gbs = prob.bytes_fwd / ms / 1e6
+                out[wl.name] = {"step_us": 1e3 * ms, "tokens_per_s": wl.B / (ms / 1e3), "fwd_bytes": prob.bytes_fwd,
+                                "fwd_gbs": gbs, "fwd_hbm_frac": gbs / hbm_peak,
+                                "bound_us": 1e6 * prob.bytes_fwd / (hbm_peak * 1e9), "roofline_frac": gbs / hbm_peak,
+                                "timing": "200 steps queued behind a GPU sleep, back to back between two events"}
+                del prob
+                torch.cuda.empty_cache()
+                continue
             f, b = time_steps(prob, 100)
         except dsc.DscError as e:
             out[wl.name] = {"status": str(e)}

@@ -477,15 +477,40 @@ __device__ __forceinline__ void load_v(const E *p, float (&v)[V])
     load_n<E, V>(p, v);
 }
 
-template <typename E, int V>
-__global__ void decode_step_kernel(const E *__restrict__ x, const E *__restrict__ w, E *__restrict__ hist,
-                                   const int32_t *__restrict__ pos, E *__restrict__ y, int B, int D, int W, int H,
-                                   int *status)
+// The filter values of a chunk's V channels, tap k of channel v at f[v][k].  HM says how the chunk meets
+// the heads: 1 -- one head holds all V channels (H % V == 0): its W taps are read once; 2 -- every channel
+// is its own head (H == 1): V*W consecutive values; 0 -- anything else, one value at a time.
+template <typename E, int V, int HM, int WM>
+__device__ __forceinline__ void decode_filter(const E *wb, int c, int W, int H, float (&f)[V][WM])
+{
+    if constexpr (HM == 1) {
+        float t[WM];
+        const E *p = wb + (c / H) * W;
+#pragma unroll
+        for (int k = 0; k < WM; ++k) t[k] = k < W ? Elem<E>::to_f(p[k]) : 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+#pragma unroll
+            for (int k = 0; k < WM; ++k) f[v][k] = t[k];
+    } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+#pragma unroll
+            for (int k = 0; k < WM; ++k)
+                f[v][k] = k < W ? Elem<E>::to_f(wb[(HM == 2 ? (c + v) : (c + v) / H) * W + k]) : 0.f;
+    }
+}
+
+template <typename E, int V, int HM, int W>
+__global__ void __launch_bounds__(256) decode_step_kernel(const E *__restrict__ x, const E *__restrict__ w,
+                                                          E *__restrict__ hist, const int32_t *__restrict__ pos,
+                                                          E *__restrict__ y, int B, int D, int H, int *status)
 {
     grid_dependents_launch();
     grid_dependency_wait();
     const int chunks = D / V;
     const int G = D / H;
+    static_assert(W >= 1 && W <= 8, "filter width");
     const long long n = static_cast<long long>(B) * chunks;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -498,17 +523,22 @@ __global__ void decode_step_kernel(const E *__restrict__ x, const E *__restrict_
         }
         float xv[V], acc[V];
         load_v<E, V>(x + static_cast<size_t>(b) * D + c, xv);
-        const E *wb = w + static_cast<size_t>(b) * G * W;
+        float f[V][W];
+        decode_filter<E, V, HM, W>(w + static_cast<size_t>(b) * G * W, c, W, H, f);
 #pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = fmaf(Elem<E>::to_f(wb[((c + v) / H) * W]), xv[v], xv[v]);
+        for (int v = 0; v < V; ++v) acc[v] = fmaf(f[v][0], xv[v], xv[v]);
         E *hb = hist + static_cast<size_t>(b) * (W - 1) * D;
-        for (int k = 1; k < W && k <= p; ++k) {
-            const int slot = (p - k) % (W - 1);
-            float hv[V];
-            load_v<E, V>(hb + static_cast<size_t>(slot) * D + c, hv);
+        // the history rows of taps 1 .. min(pos, W-1): all loads first, then the products
+        float hv[W > 1 ? W - 1 : 1][V];
 #pragma unroll
-            for (int v = 0; v < V; ++v) acc[v] = fmaf(Elem<E>::to_f(wb[((c + v) / H) * W + k]), hv[v], acc[v]);
-        }
+        for (int k = 1; k < W; ++k)
+            if (k <= p) load_v<E, V>(hb + static_cast<size_t>((p - k) % (W - 1)) * D + c, hv[k - 1]);
+#pragma unroll
+        for (int k = 1; k < W; ++k)
+            if (k <= p) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[v] = fmaf(f[v][k], hv[k - 1][v], acc[v]);
+            }
         store_n<E, V>(y + static_cast<size_t>(b) * D + c, acc);
         // every history read of this chunk is done: this token's input takes the oldest slot
         if (W > 1) store_n<E, V>(hb + static_cast<size_t>(p % (W - 1)) * D + c, xv);
@@ -628,6 +658,19 @@ dsc_status static_bwd(const StaticArgs &a)
     return a.dt == DSC_BF16 ? static_bwd_t<__nv_bfloat16>(a, dev) : static_bwd_t<float>(a, dev);
 }
 
+template <typename E, int V, int W>
+static dsc_status decode_launch(const DecodeArgs &a, unsigned nb, int *st, bool vec)
+{
+    const E *x = static_cast<const E *>(a.x), *w = static_cast<const E *>(a.w);
+    E *h = static_cast<E *>(a.hist), *y = static_cast<E *>(a.y);
+    if (!vec) return launch_overlapped(decode_step_kernel<E, 1, 0, W>, nb, 256u, 0, a.stream, x, w, h, a.pos, y, a.B, a.D, a.H, st);
+    if (a.H % V == 0)
+        return launch_overlapped(decode_step_kernel<E, V, 1, W>, nb, 256u, 0, a.stream, x, w, h, a.pos, y, a.B, a.D, a.H, st);
+    if (a.H == 1)
+        return launch_overlapped(decode_step_kernel<E, V, 2, W>, nb, 256u, 0, a.stream, x, w, h, a.pos, y, a.B, a.D, a.H, st);
+    return launch_overlapped(decode_step_kernel<E, V, 0, W>, nb, 256u, 0, a.stream, x, w, h, a.pos, y, a.B, a.D, a.H, st);
+}
+
 template <typename E>
 static dsc_status decode_t(const DecodeArgs &a, const DeviceInfo &dev)
 {
@@ -638,13 +681,18 @@ static dsc_status decode_t(const DecodeArgs &a, const DeviceInfo &dev)
     if (blocks > static_cast<long long>(dev.sm_count) * 16) blocks = static_cast<long long>(dev.sm_count) * 16;
     int *st = device_status_word();
     if (!st) return DSC_ERR_CUDA;
-    if (vec)
-        return launch_overlapped(decode_step_kernel<E, V>, static_cast<unsigned>(blocks), 256u, 0, a.stream,
-                                 static_cast<const E *>(a.x), static_cast<const E *>(a.w), static_cast<E *>(a.hist),
-                                 a.pos, static_cast<E *>(a.y), a.B, a.D, a.W, a.H, st);
-    return launch_overlapped(decode_step_kernel<E, 1>, static_cast<unsigned>(blocks), 256u, 0, a.stream,
-                             static_cast<const E *>(a.x), static_cast<const E *>(a.w), static_cast<E *>(a.hist), a.pos,
-                             static_cast<E *>(a.y), a.B, a.D, a.W, a.H, st);
+    const unsigned nb = static_cast<unsigned>(blocks);
+    switch (a.W) {
+    case 1: return decode_launch<E, V, 1>(a, nb, st, vec);
+    case 2: return decode_launch<E, V, 2>(a, nb, st, vec);
+    case 3: return decode_launch<E, V, 3>(a, nb, st, vec);
+    case 4: return decode_launch<E, V, 4>(a, nb, st, vec);
+    case 5: return decode_launch<E, V, 5>(a, nb, st, vec);
+    case 6: return decode_launch<E, V, 6>(a, nb, st, vec);
+    case 7: return decode_launch<E, V, 7>(a, nb, st, vec);
+    case 8: return decode_launch<E, V, 8>(a, nb, st, vec);
+    default: return DSC_ERR_INVALID_ARG;
+    }
 }
 
 dsc_status decode_step(const DecodeArgs &a)
