@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--row", default=None, help="only measure this one row of the per-workload table and print it")
     return ap.parse_args()
 
 
@@ -523,6 +524,15 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     from dynamic_short_convolution_gb300 import inputs
 
+    if args.row is not None:  # one row of the table alone (for profiling one workload's kernels)
+        import torch
+
+        inputs.by_name(args.row)
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        hbm_peak, tc_peak, _, _ = peaks()
+        print(json.dumps({"rows": measure_rows(dev, hbm_peak, tc_peak, only=args.row)}), flush=True)
+        return 0
     wl = inputs.by_name(args.workload)
     if wl.kind == "decode":
         raise SystemExit("the decode step has no backward pass: it is measured in the rows table only")
@@ -697,8 +707,9 @@ def measure_e2e(prob, steps, dev, world):
                    "steps pipelined on three streams"}
 
 
-def measure_rows(dev, hbm_peak, tc_peak):
-    """Every workload, timed the same way (fewer steps): fwd / bwd device time and roofline fractions."""
+def measure_rows(dev, hbm_peak, tc_peak, only=None):
+    """Every workload (or the one named `only`), timed the same way (fewer steps): fwd / bwd device time and
+    roofline fractions."""
     import torch
 
     import dynamic_short_convolution_gb300 as dsc
@@ -706,6 +717,8 @@ def measure_rows(dev, hbm_peak, tc_peak):
 
     out = {}
     for wid, wl in inputs.WORKLOADS.items():
+        if only is not None and wl.name != only:
+            continue
         try:
             prob = make_problem(wl, dev)
             for _ in range(3):
