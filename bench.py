@@ -369,6 +369,26 @@ def make_problem(wl, dev):
     return {"lowrank": LowrankProblem, "static": StaticProblem, "decode": DecodeProblem}.get(wl.kind, DenseProblem)(wl, dev)
 
 
+def time_graph_replay(prob, steps):
+    """Device time per forward call (ms) when `steps` calls (over the rotating copies) are recorded in one
+    CUDA graph and replayed, as a serving loop runs them."""
+    import torch
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            prob.advance()
+            prob.fwd()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def time_back_to_back(prob, steps):
     """Device time per forward call (ms) for a kernel shorter than the host's launch path: a GPU sleep
     lets the host queue every call first, then they run back to back between two events."""
@@ -728,11 +748,14 @@ def measure_rows(dev, hbm_peak, tc_peak, only=None):
             torch.cuda.synchronize()
             if wl.kind == "decode":
                 ms = time_back_to_back(prob, 200)
+                gms = time_graph_replay(prob, 200)
                 gbs = prob.bytes_fwd / ms / 1e6
                 out[wl.name] = {"step_us": 1e3 * ms, "tokens_per_s": wl.B / (ms / 1e3), "fwd_bytes": prob.bytes_fwd,
                                 "fwd_gbs": gbs, "fwd_hbm_frac": gbs / hbm_peak,
                                 "bound_us": 1e6 * prob.bytes_fwd / (hbm_peak * 1e9), "roofline_frac": gbs / hbm_peak,
-                                "timing": "200 steps queued behind a GPU sleep, back to back between two events"}
+                                "timing": "200 steps queued behind a GPU sleep, back to back between two events",
+                                "graph_step_us": 1e3 * gms, "graph_hbm_frac": prob.bytes_fwd / gms / 1e6 / hbm_peak,
+                                "graph_timing": "the same 200 steps recorded in one CUDA graph, one replay timed"}
                 del prob
                 torch.cuda.empty_cache()
                 continue

@@ -516,32 +516,43 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const E *__restrict__ 
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int b = static_cast<int>(i / chunks);
         const int c = static_cast<int>(i - static_cast<long long>(b) * chunks) * V;
+        // every ring slot is loaded at once, before the position is known (the addresses do not depend on
+        // it); slot s then holds tap k = (pos - s) mod (W-1) (W-1 where that is 0), used when k <= pos
+        E *hb = hist + static_cast<size_t>(b) * (W - 1) * D + c;
+        float hv[W > 1 ? W - 1 : 1][V];
+#pragma unroll
+        for (int sl = 0; sl + 1 < W; ++sl) load_v<E, V>(hb + static_cast<size_t>(sl) * D, hv[sl]);
+        float xv[V], acc[V];
+        load_v<E, V>(x + static_cast<size_t>(b) * D + c, xv);
+        float f[V][W];
+        decode_filter<E, V, HM, W>(w + static_cast<size_t>(b) * G * W, c, W, H, f);
         int p = pos[b];
         if (p < 0) {  // not a position: treated as a document start, and reported
             record_status(status, kStatusInvalid);
             p = 0;
         }
-        float xv[V], acc[V];
-        load_v<E, V>(x + static_cast<size_t>(b) * D + c, xv);
-        float f[V][W];
-        decode_filter<E, V, HM, W>(w + static_cast<size_t>(b) * G * W, c, W, H, f);
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[v] = fmaf(f[v][0], xv[v], xv[v]);
-        E *hb = hist + static_cast<size_t>(b) * (W - 1) * D;
-        // the history rows of taps 1 .. min(pos, W-1): all loads first, then the products
-        float hv[W > 1 ? W - 1 : 1][V];
+        if constexpr (W > 1) {
+            const int pm = p % (W - 1);
 #pragma unroll
-        for (int k = 1; k < W; ++k)
-            if (k <= p) load_v<E, V>(hb + static_cast<size_t>((p - k) % (W - 1)) * D + c, hv[k - 1]);
+            for (int sl = 0; sl + 1 < W; ++sl) {
+                int k = pm - sl;
+                k = k <= 0 ? k + (W - 1) : k;  // 1 .. W-1
+                if (k <= p) {
 #pragma unroll
-        for (int k = 1; k < W; ++k)
-            if (k <= p) {
+                    for (int v = 0; v < V; ++v) {
+                        float fk = f[v][1];
 #pragma unroll
-                for (int v = 0; v < V; ++v) acc[v] = fmaf(f[v][k], hv[k - 1][v], acc[v]);
+                        for (int kk = 2; kk < W; ++kk) fk = k == kk ? f[v][kk] : fk;
+                        acc[v] = fmaf(fk, hv[sl][v], acc[v]);
+                    }
+                }
             }
+        }
         store_n<E, V>(y + static_cast<size_t>(b) * D + c, acc);
         // every history read of this chunk is done: this token's input takes the oldest slot
-        if (W > 1) store_n<E, V>(hb + static_cast<size_t>(p % (W - 1)) * D + c, xv);
+        if (W > 1) store_n<E, V>(hb + static_cast<size_t>(p % (W - 1)) * D, xv);
     }
 }
 
