@@ -389,6 +389,23 @@ def time_graph_replay(prob, steps):
     return e0.elapsed_time(e1) / steps
 
 
+def time_steps_back_to_back(prob, steps):
+    """Device time per fwd + bwd step (ms) for steps shorter than the host's launch path: every step is
+    queued behind a GPU sleep first, then they run back to back between two events."""
+    import torch
+
+    torch.cuda._sleep(int(2e6) + steps * 120000)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        prob.advance()
+        prob.fwd()
+        prob.bwd()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def time_back_to_back(prob, steps):
     """Device time per forward call (ms) for a kernel shorter than the host's launch path: a GPU sleep
     lets the host queue every call first, then they run back to back between two events."""
@@ -781,6 +798,10 @@ def measure_rows(dev, hbm_peak, tc_peak, only=None):
         else:
             r["bound_us"] = 1e6 * (prob.bytes_fwd + prob.bytes_bwd) / (hbm_peak * 1e9)
             r["roofline_frac"] = r["fwdbwd_hbm_frac"]
+        if (mf + mb) * 1e3 < 60.0:  # a step this short is host-bound between events: its device time too
+            ms = time_steps_back_to_back(prob, 100)
+            r["step_us_back_to_back"] = 1e3 * ms
+            r["tokens_per_s_back_to_back"] = wl.B * wl.T / (ms / 1e3)
         out[wl.name] = r
         del prob
         torch.cuda.empty_cache()
