@@ -27,14 +27,16 @@ namespace dsc {
 
 namespace stc {
 
-// Tokens per tile and per consumer warp.  Forward: 16 warps (bf16) of 6 tokens, as the materialised
-// forward.  Backward: 8 warps of 6 tokens -- the dx ring, the x window, the filter and the dw partials all
-// live in registers.
+// Tokens per tile and per consumer warp, and the depth of the stage ring (from measured sweeps on GB300).
+// Forward: 16 warps (bf16) of 3 tokens, tiles of 48 tokens, up to 8 stages in flight.  Backward: 8 warps
+// of 6 tokens -- the dx ring, the x window, the filter and the dw partials all live in registers -- and up
+// to 4 stages (a deeper ring of smaller tiles was slower).
 template <typename E, bool BWD>
 struct Tile {
-    static constexpr int TT = (sizeof(E) == 2 ? 96 : 48) / (BWD ? 2 : 1);
-    static constexpr int RPW = 6;
+    static constexpr int TT = (sizeof(E) == 2 ? 48 : 24);
+    static constexpr int RPW = BWD ? 6 : 3;
     static constexpr int NCW = TT / RPW;
+    static constexpr int kStageCap = BWD ? 4 : 8;
 };
 
 struct Params {
@@ -59,7 +61,8 @@ struct Plan {
 };
 
 // Lay out the stages; false when the TMA path cannot take the arguments (the scalar path does).
-inline bool make_plan(const StaticArgs &a, bool bwd, int TT, int NCW, int W, const DeviceInfo &dev, Plan *p)
+inline bool make_plan(const StaticArgs &a, bool bwd, int TT, int NCW, int W, int stage_cap, const DeviceInfo &dev,
+                      Plan *p)
 {
     const int es = a.dt == DSC_BF16 ? 2 : 4;
     if (a.D % 8 != 0) return false;  // whole 8-channel lane vectors
@@ -81,7 +84,7 @@ inline bool make_plan(const StaticArgs &a, bool bwd, int TT, int NCW, int W, con
     const unsigned header = 2048;
     const int fit = static_cast<int>((static_cast<unsigned>(dev.max_smem_optin) - header) / p->stage_bytes);
     if (fit < 2) return false;
-    p->nstages = fit < 4 ? fit : 4;
+    p->nstages = fit < stage_cap ? fit : stage_cap;
     // the backward's dw reduction reuses the stages: NCW partials of kDC * W fp32 values
     if (bwd && static_cast<unsigned>(NCW * kDC * W * 4) > p->nstages * p->stage_bytes) return false;
     p->smem = header + p->nstages * p->stage_bytes;
@@ -563,7 +566,7 @@ static dsc_status launch_static_fwd(const StaticArgs &a, const DeviceInfo &dev)
 {
     using Tl = stc::Tile<E, false>;
     stc::Plan pl;
-    if (!stc::make_plan(a, false, Tl::TT, Tl::NCW, W, dev, &pl)) return DSC_ERR_UNSUPPORTED;
+    if (!stc::make_plan(a, false, Tl::TT, Tl::NCW, W, Tl::kStageCap, dev, &pl)) return DSC_ERR_UNSUPPORTED;
     const CUtensorMapDataType tdt = sizeof(E) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const unsigned long long BT = static_cast<unsigned long long>(a.B) * a.T;
     CUtensorMap tm_x;
@@ -581,7 +584,7 @@ static dsc_status launch_static_bwd(const StaticArgs &a, const DeviceInfo &dev)
 {
     using Tl = stc::Tile<E, true>;
     stc::Plan pl;
-    if (!stc::make_plan(a, true, Tl::TT, Tl::NCW, W, dev, &pl)) return DSC_ERR_UNSUPPORTED;
+    if (!stc::make_plan(a, true, Tl::TT, Tl::NCW, W, Tl::kStageCap, dev, &pl)) return DSC_ERR_UNSUPPORTED;
     const CUtensorMapDataType tdt = sizeof(E) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const unsigned long long BT = static_cast<unsigned long long>(a.B) * a.T;
     const unsigned long long row = static_cast<unsigned long long>(a.D) * sizeof(E);
