@@ -272,7 +272,7 @@ static dsc_status launch_bwd_tma(const DenseArgs &a, const DeviceInfo &dev)
 {
     using Cfg = TileCfg<E, HPT, true>;
     DensePlan plan;
-    if (!make_dense_plan(a, true, Cfg::TT, Cfg::RPW, dev, &plan)) return DSC_ERR_UNSUPPORTED;
+    if (!make_dense_plan(a, true, Cfg::TT, Cfg::RPW, Cfg::kStageCap, dev, &plan)) return DSC_ERR_UNSUPPORTED;
     const CUtensorMapDataType tdt =
         sizeof(E) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const unsigned long long BT = static_cast<unsigned long long>(a.B) * a.T;

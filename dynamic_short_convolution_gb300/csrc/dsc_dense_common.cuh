@@ -20,19 +20,25 @@ constexpr int kMaxStages = 8;   // shared-memory ring depth cap
 
 // Tokens per tile (TT) and per consumer warp (RPW), by element type, heads
 // per lane (HPT: 8 for H=1, 4 for H=2, 2 for H=4, 1 for H>=8) and direction.
-// bf16 forward: 16 consumer warps, stages of 60-85 KB (2-3 in flight).  bf16
-// backward: 16 consumer warps of 3 tokens for H >= 8 (stages of ~45 KB, 4 in
-// flight), 4 warps of 4 tokens for H = 1 (the filter rows dominate a stage).
-// Chosen by measured sweeps of the tile shape on GB300.  fp32 halves the tokens.
-template <typename E, int HPT, bool BWD>
+// bf16 forward: 16 consumer warps; for H >= 8 tiles of 48 tokens (3 per warp,
+// stages of ~28 KB, a ring of 5) or, with WIDE, of 64 tokens (4 per warp,
+// stages of ~36 KB, a ring of 6) -- the launcher picks one per call; for
+// smaller H larger tiles (the filter rows grow with 1/H).  bf16 backward: 16
+// consumer warps of 3 tokens for H >= 8 (stages of ~45 KB), 4 warps of 4
+// tokens for H = 1 (the filter rows dominate a stage).  Chosen by measured
+// sweeps and A/B runs of the tile shape and ring depth on GB300.  fp32 halves
+// the tokens.
+template <typename E, int HPT, bool BWD, bool WIDE = false>
 struct TileCfg {
     static constexpr bool kBf16 = sizeof(E) == 2;
     static constexpr int TTb = BWD ? (HPT == 1 ? 48 : HPT == 8 ? 16 : 32)
-                                   : (HPT == 1 ? 96 : HPT == 2 ? 64 : HPT == 4 ? 48 : 32);
-    static constexpr int RPWb = BWD ? (HPT == 1 ? 3 : 4) : (HPT == 1 ? 6 : HPT == 2 ? 4 : HPT == 4 ? 3 : 2);
+                                   : (HPT == 1 ? (WIDE ? 64 : 48) : HPT == 2 ? 64 : HPT == 4 ? 48 : 32);
+    static constexpr int RPWb = BWD ? (HPT == 1 ? 3 : 4)
+                                    : (HPT == 1 ? (WIDE ? 4 : 3) : HPT == 2 ? 4 : HPT == 4 ? 3 : 2);
     static constexpr int TT = kBf16 ? TTb : (BWD && HPT == 8 ? 8 : TTb / 2);
     static constexpr int RPW = kBf16 ? RPWb : (BWD ? (HPT == 1 ? 8 : 4) : RPWb);
     static constexpr int NCW = TT / RPW;  // consumer warps
+    static constexpr int kStageCap = (!BWD && HPT == 1 && kBf16 && !WIDE) ? 5 : kMaxStages;
     static_assert(TT % RPW == 0, "whole warps per tile");
 };
 
@@ -75,7 +81,8 @@ inline int ilog2_exact(int v)
 
 // Decide whether the TMA path can take these arguments and lay out its stages.
 // Returns false (use the scalar path) when a TMA alignment or size rule fails.
-inline bool make_dense_plan(const DenseArgs &a, bool bwd, int TT, int RPW, const DeviceInfo &dev, DensePlan *p)
+inline bool make_dense_plan(const DenseArgs &a, bool bwd, int TT, int RPW, int stage_cap, const DeviceInfo &dev,
+                            DensePlan *p)
 {
     const int esize = (a.dt == DSC_BF16) ? 2 : 4;
     p->esize = esize;
@@ -122,8 +129,7 @@ inline bool make_dense_plan(const DenseArgs &a, bool bwd, int TT, int RPW, const
     const unsigned header = 2048;  // barriers + abort flag, then slack to align the stages to 1024 B
     const int fit = static_cast<int>((static_cast<unsigned>(dev.max_smem_optin) - header) / p->stage_bytes);
     if (fit < 2) return false;
-    p->nstages = fit < kMaxStages ? fit : kMaxStages;
-    if (p->nstages > 4) p->nstages = 4;
+    p->nstages = fit < stage_cap ? fit : stage_cap;
     p->smem_bytes = header + p->nstages * p->stage_bytes;
     const long long BT = static_cast<long long>(a.B) * a.T;
     p->n_cb = (a.D + kDC - 1) / kDC;

@@ -57,6 +57,10 @@ SMALL = [
     (1, 65, 512, 1, 1, "bf16", False, 0, 0),      # W = 1
     (2, 90, 128, 4, 1, "f32", True, 1, 25),
     (4, 33, 2048, 4, 16, "bf16", True, 4, 20),
+    # bf16 with H >= 8 and enough tiles that 64-token tiles balance a 152-SM grid at least as well as
+    # 48-token ones: the forward launcher takes its 64-token tile variant (the second with a ragged tail)
+    (2, 4864, 256, 4, 16, "bf16", True, 1, 40),
+    (1, 9700, 512, 3, 8, "bf16", False, 0, 0),
 ]
 
 
