@@ -21,11 +21,11 @@ constexpr int kMaxStages = 8;   // shared-memory ring depth cap
 // Tokens per tile (TT) and per consumer warp (RPW), by element type, heads
 // per lane (HPT: 8 for H=1, 4 for H=2, 2 for H=4, 1 for H>=8) and direction.
 // bf16 forward: 16 consumer warps; for H >= 8 tiles of 48 tokens (3 per warp,
-// stages of ~28 KB, a ring of 5) or, with WIDE, of 64 tokens (4 per warp,
-// stages of ~36 KB, a ring of 6) -- the launcher picks one per call; for
+// stages of 33 KB, a ring of 5) or, with WIDE, of 64 tokens (4 per warp,
+// stages of 43 KB, 5 of them fit) -- the launcher picks one per call; for
 // smaller H larger tiles (the filter rows grow with 1/H).  bf16 backward: 16
-// consumer warps of 3 tokens for H >= 8 (stages of ~45 KB), 4 warps of 4
-// tokens for H = 1 (the filter rows dominate a stage).  Chosen by measured
+// consumer warps of 3 tokens for H >= 8, 4 warps of 4 tokens for H = 1 (the
+// filter rows dominate a stage); stages of 59 KB, 3 fit.  Chosen by measured
 // sweeps and A/B runs of the tile shape and ring depth on GB300.  fp32 halves
 // the tokens.
 template <typename E, int HPT, bool BWD, bool WIDE = false>
