@@ -414,10 +414,15 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                     }
                     // this warp's filter columns (bias included) of the step: group gl, column c*W + k
                     uint32_t acc[GPW][8 * W];
+                    uint4 gpre[GPW];  // dy of this token, read from shared memory while the TMEM load is in flight
                     if (active) {
 #pragma unroll
                         for (int gi = 0; gi < GPW; ++gi)
                             tmem_ld_cols<8 * W>(lane_base + kColW + (c * GPW + gi) * 8 * W, acc[gi]);
+#pragma unroll
+                        for (int gi = 0; gi < GPW; ++gi)
+                            gpre[gi] = *reinterpret_cast<const uint4 *>(
+                                dys + swz_b<RB>(row, (j * SCB + (c * GPW + gi) * 8) >> 3));
                     }
                     tmem_ld_wait();
                     tc_fence_before();
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(lrb::kThreads, 1)
                             float gy[8];  // dy of this token
                             float dxv[8];
                             {
-                                const uint4 gr = *reinterpret_cast<const uint4 *>(dys + dy_off);
+                                const uint4 gr = gpre[gi];
                                 const uint32_t wv[4] = {gr.x, gr.y, gr.z, gr.w};
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
