@@ -152,6 +152,50 @@ def make(wl: Workload, with_grad: bool = True) -> dict:
     return out
 
 
+def _normal_on(device, shape, std, wid, idx, dtype):
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 * wid + idx)
+    t = torch.randn(*shape, generator=g, dtype=torch.float32, device=device)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def make_on_device(wl: Workload, device, with_grad: bool = True) -> dict:
+    """All inputs of one workload drawn directly on a CUDA device: the same seeds and distributions as
+    ``make``/``make_decode`` through torch's device generator (so different values), for shapes whose host
+    draw and copy would take minutes.  Document offsets and decode positions are drawn on the host as in
+    ``make`` and copied over."""
+    dt = wl.torch_dtype
+    out = {}
+    if wl.kind == "decode":
+        host = make_decode(replace(wl, D=8, H=1))  # positions only: they depend on B and the seed, not on D
+        out["x"] = _normal_on(device, (wl.B, wl.D), 1.0, wl.wid, X, dt)
+        w = _normal_on(device, (wl.B, wl.D // wl.H, wl.W), wl.w_std, wl.wid, WGT, torch.float32)
+        if wl.w_tap0:
+            w[..., 0] += wl.w_tap0
+        out["w"] = w.to(dt)
+        out["hist"] = _normal_on(device, (wl.B, wl.W - 1, wl.D), 1.0, wl.wid, HIST, dt)
+        out["pos"] = host["pos"].to(device)
+        return out
+    out["x"] = _normal_on(device, (wl.B, wl.T, wl.D), 1.0, wl.wid, X, dt)
+    if wl.kind in ("static", "dense"):
+        shape = (wl.D, wl.W) if wl.kind == "static" else (wl.B, wl.T, wl.D // wl.H, wl.W)
+        w = _normal_on(device, shape, wl.w_std, wl.wid, WGT, torch.float32)
+        if wl.w_tap0:
+            w[..., 0] += wl.w_tap0
+        out["w"] = w.to(dt)
+    else:
+        out["z"] = _normal_on(device, (wl.B, wl.T, wl.R), 1.0, wl.wid, Z, dt)
+        out["U"] = _normal_on(device, (wl.R, wl.D * wl.W), 1.0 / math.sqrt(wl.R), wl.wid, U, dt)
+        out["bias"] = _normal_on(device, (wl.D * wl.W,), 0.1, wl.wid, BIAS, torch.float32)
+    if with_grad:
+        out["dy"] = _normal_on(device, (wl.B, wl.T, wl.D), 1.0, wl.wid, DY, dt)
+    cu = doc_offsets(wl)
+    out["cu_seqlens"] = None if cu is None else cu.to(device)
+    return out
+
+
 def make_decode(wl: Workload) -> dict:
     """One decode step's inputs: x [B, D], w [B, D/H, W], hist [B, W-1, D] (a ring of past inputs),
     pos [B] int32 (each token's position in its document; about a fifth below W-1)."""
