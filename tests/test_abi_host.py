@@ -40,6 +40,35 @@ def test_every_declared_symbol_is_exported(L):
         assert n in _abi.SIGNATURES, f"binding has no signature for {n}"
 
 
+def test_header_compiles_as_c_and_links(L, tmp_path):
+    """A plain C99 program includes the header, links libdsc.so and gets an argument error back (no GPU call)."""
+    import shutil
+    import subprocess
+
+    from dynamic_short_convolution_gb300 import build
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(build.nvcc()))), "include")
+    src = tmp_path / "use_dsc.c"
+    src.write_text(
+        "#include <stdio.h>\n#include \"dsc.h\"\n"
+        "int main(void) {\n"
+        "    dsc_status s = dsc_fwd(0, 0, 0, 0, 8, 64, 4, 1, DSC_BF16, 0, 0, 0);\n"
+        "    printf(\"%d %s\\n\", dsc_version(), dsc_status_string(s));\n"
+        "    return s == DSC_ERR_INVALID_ARG ? 0 : 1;\n"
+        "}\n")
+    exe = tmp_path / "use_dsc"
+    libdir = os.path.dirname(build.LIB)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror=implicit-function-declaration", "-I",
+                        os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe), "-L", libdir,
+                        "-ldsc", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and "DSC_ERR_INVALID_ARG" in r.stdout, r.stdout + r.stderr
+
+
 def test_status_strings(L):
     assert L.dsc_status_string(0) == b"DSC_OK"
     assert L.dsc_status_string(4) == b"DSC_ERR_TIMEOUT"
