@@ -28,9 +28,10 @@ float64 numpy arrays.  ``rows`` restricts per-token outputs to a token
 range ``(r0, r1)`` of the flattened B*T axis; ``cols`` restricts the
 low-rank parameter gradients to a list of filter columns.
 
-Parity status: every function here is pinned by ``tests/test_oracle.py``
-(library conv1d, closed forms, invariants, finite differences, adjoint
-identities and a hand-computed golden fixture).
+Parity status: every function here is pinned, by ``tests/test_oracle.py`` and
+``tests/test_oracle_static_decode.py`` (library conv1d, closed forms,
+invariants, finite differences, adjoint identities, a decode chain equal to
+the full forward, and a hand-computed golden fixture).
 """
 from __future__ import annotations
 
