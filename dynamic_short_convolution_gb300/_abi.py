@@ -86,9 +86,16 @@ def _dt(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None, device=None) -> int:
+    """Device pointer of a contiguous CUDA tensor, after checking its dtype, exact shape and device: the
+    library trusts the sizes it is given, so a tensor of the wrong size would be read or written past its
+    end on the GPU."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's tensors are on {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -96,15 +103,29 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
     return t.data_ptr()
 
 
+def _lead(x: torch.Tensor, name: str, ndim: int) -> torch.device:
+    """The device of the call: the lead tensor's, which must be the current CUDA device (the library
+    launches on the current device)."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if x.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(x.shape)}")
+    if x.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {x.device} but the current device is cuda:{torch.cuda.current_device()}")
+    return x.device
+
+
 def _stream(stream) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
 
 
-def _cu(cu_seqlens):
+def _cu(cu_seqlens, device=None):
     if cu_seqlens is None:
         return None, 0
-    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    if not isinstance(cu_seqlens, torch.Tensor) or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D tensor of at least 2 offsets")
+    _dev(cu_seqlens, "cu_seqlens", torch.int32, device=device)
     return cu_seqlens.data_ptr(), cu_seqlens.numel() - 1
 
 
@@ -114,46 +135,60 @@ def dsc_version() -> int:
 
 def dsc_fwd(x, w, y=None, *, cu_seqlens=None, stream=None):
     """y = x + dynamic conv(x) with w [B,T,D/H,W] (materialised H=1 or head-wise)."""
+    dev = _lead(x, "x", 3)
     B, T, D = x.shape
-    G, W = w.shape[2], w.shape[3]
-    if tuple(w.shape[:2]) != (B, T) or G < 1 or D % G:
+    if w.dim() != 4 or tuple(w.shape[:2]) != (B, T) or w.shape[2] < 1 or D % w.shape[2]:
         raise ValueError("w must be [B, T, D/H, W]")
+    G, W = w.shape[2], w.shape[3]
     if y is None:
         y = torch.empty_like(x)
-    cu, n = _cu(cu_seqlens)
-    s = lib().dsc_fwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(y, "y", x.dtype), B, T, D, W, D // G, _dt(x),
-                      cu, n, _stream(stream))
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_fwd(_dev(x, "x"), _dev(w, "w", x.dtype, device=dev), _dev(y, "y", x.dtype, x.shape, dev), B, T, D,
+                      W, D // G, _dt(x), cu, n, _stream(stream))
     _check(s, "dsc_fwd")
     return y
 
 
 def dsc_bwd(x, w, dy, dx=None, dw=None, *, cu_seqlens=None, stream=None):
     """(dx, dw) of the forward pass for the upstream gradient dy."""
+    dev = _lead(x, "x", 3)
     B, T, D = x.shape
-    G, W = w.shape[2], w.shape[3]
-    if tuple(w.shape[:2]) != (B, T) or G < 1 or D % G or tuple(dy.shape) != (B, T, D):
+    if w.dim() != 4 or tuple(w.shape[:2]) != (B, T) or w.shape[2] < 1 or D % w.shape[2]:
         raise ValueError("shapes: x, dy [B,T,D]; w [B,T,D/H,W]")
+    G, W = w.shape[2], w.shape[3]
     dx = torch.empty_like(x) if dx is None else dx
     dw = torch.empty_like(w) if dw is None else dw
-    cu, n = _cu(cu_seqlens)
-    s = lib().dsc_bwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(dy, "dy", x.dtype), _dev(dx, "dx", x.dtype),
-                      _dev(dw, "dw", x.dtype), B, T, D, W, D // G, _dt(x), cu, n, _stream(stream))
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_bwd(_dev(x, "x"), _dev(w, "w", x.dtype, device=dev), _dev(dy, "dy", x.dtype, x.shape, dev),
+                      _dev(dx, "dx", x.dtype, x.shape, dev), _dev(dw, "dw", x.dtype, w.shape, dev), B, T, D, W,
+                      D // G, _dt(x), cu, n, _stream(stream))
     _check(s, "dsc_bwd")
     return dx, dw
 
 
-def dsc_lowrank_fwd(x, z, U, bias, y=None, *, cu_seqlens=None, stream=None):
-    """y = x + dynamic conv(x) with the filter zU + bias formed on chip."""
+def _lowrank_dims(x, z, U, bias):
+    """(device, (B, T, D, W, R)) of a low-rank call: x [B,T,D], z [B,T,R], U [R, D*W], bias [D*W]."""
+    dev = _lead(x, "x", 3)
     B, T, D = x.shape
-    R = z.shape[-1]
-    if U.shape[0] != R or U.shape[1] % D:
+    if not isinstance(z, torch.Tensor) or z.dim() != 3 or tuple(z.shape[:2]) != (B, T):
+        raise ValueError("z must be [B, T, R]")
+    R = z.shape[2]
+    if not isinstance(U, torch.Tensor) or U.dim() != 2 or U.shape[0] != R or U.shape[1] % D:
         raise ValueError("U must be [R, D*W]")
     W = U.shape[1] // D
+    if not isinstance(bias, torch.Tensor) or tuple(bias.shape) != (D * W,):
+        raise ValueError("bias must be [D*W]")
+    return dev, (B, T, D, W, R)
+
+
+def dsc_lowrank_fwd(x, z, U, bias, y=None, *, cu_seqlens=None, stream=None):
+    """y = x + dynamic conv(x) with the filter zU + bias formed on chip."""
+    dev, (B, T, D, W, R) = _lowrank_dims(x, z, U, bias)
     y = torch.empty_like(x) if y is None else y
-    cu, n = _cu(cu_seqlens)
-    s = lib().dsc_lowrank_fwd(_dev(x, "x"), _dev(z, "z", x.dtype), _dev(U, "U", x.dtype),
-                              _dev(bias, "bias", torch.float32), _dev(y, "y", x.dtype), B, T, D, W, R, _dt(x), cu,
-                              n, _stream(stream))
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_lowrank_fwd(_dev(x, "x"), _dev(z, "z", x.dtype, device=dev), _dev(U, "U", x.dtype, device=dev),
+                              _dev(bias, "bias", torch.float32, device=dev), _dev(y, "y", x.dtype, x.shape, dev), B,
+                              T, D, W, R, _dt(x), cu, n, _stream(stream))
     _check(s, "dsc_lowrank_fwd")
     return y
 
@@ -165,9 +200,7 @@ def dsc_lowrank_bwd_workspace_bytes(B, T, D, W, R) -> int:
 def dsc_lowrank_bwd(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=None, workspace=None, *, cu_seqlens=None,
                     stream=None):
     """(dx, dz, dU, db) of the low-rank forward pass; dU and db are fp32."""
-    B, T, D = x.shape
-    R = z.shape[-1]
-    W = U.shape[1] // D
+    dev, (B, T, D, W, R) = _lowrank_dims(x, z, U, bias)
     dx = torch.empty_like(x) if dx is None else dx
     dz = torch.empty_like(z) if dz is None else dz
     dU = torch.empty(U.shape, dtype=torch.float32, device=x.device) if dU is None else dU
@@ -175,12 +208,19 @@ def dsc_lowrank_bwd(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=None, works
     nbytes = dsc_lowrank_bwd_workspace_bytes(B, T, D, W, R)
     if workspace is None and nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
-    ws = None if not nbytes else _dev(workspace, "workspace")
-    cu, n = _cu(cu_seqlens)
-    s = lib().dsc_lowrank_bwd(_dev(x, "x"), _dev(z, "z", x.dtype), _dev(U, "U", x.dtype),
-                              _dev(bias, "bias", torch.float32), _dev(dy, "dy", x.dtype), _dev(dx, "dx", x.dtype),
-                              _dev(dz, "dz", x.dtype), _dev(dU, "dU", torch.float32),
-                              _dev(db, "db", torch.float32), ws, B, T, D, W, R, _dt(x), cu, n, _stream(stream))
+    ws = None
+    if nbytes:
+        ws = _dev(workspace, "workspace", device=dev)
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, "
+                             f"the call needs {nbytes}")
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_lowrank_bwd(_dev(x, "x"), _dev(z, "z", x.dtype, device=dev), _dev(U, "U", x.dtype, device=dev),
+                              _dev(bias, "bias", torch.float32, device=dev), _dev(dy, "dy", x.dtype, x.shape, dev),
+                              _dev(dx, "dx", x.dtype, x.shape, dev), _dev(dz, "dz", x.dtype, z.shape, dev),
+                              _dev(dU, "dU", torch.float32, U.shape, dev),
+                              _dev(db, "db", torch.float32, bias.shape, dev), ws, B, T, D, W, R, _dt(x), cu, n,
+                              _stream(stream))
     _check(s, "dsc_lowrank_bwd")
     return dx, dz, dU, db
 
@@ -190,48 +230,51 @@ def dsc_lowrank_bwd_noalloc(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=Non
     """dsc_lowrank_bwd without a caller workspace, for callers that cannot allocate device memory for one:
     the library's own fixed 8 MiB device array holds the partial sums (B*T*R <= 2,097,152; calls that
     overlap on the GPU race on it).  The output tensors, when not given, are allocated here by torch."""
-    B, T, D = x.shape
-    R = z.shape[-1]
-    W = U.shape[1] // D
+    dev, (B, T, D, W, R) = _lowrank_dims(x, z, U, bias)
     dx = torch.empty_like(x) if dx is None else dx
     dz = torch.empty_like(z) if dz is None else dz
     dU = torch.empty(U.shape, dtype=torch.float32, device=x.device) if dU is None else dU
     db = torch.empty(bias.shape, dtype=torch.float32, device=x.device) if db is None else db
-    cu, n = _cu(cu_seqlens)
-    s = lib().dsc_lowrank_bwd_noalloc(_dev(x, "x"), _dev(z, "z", x.dtype), _dev(U, "U", x.dtype),
-                                      _dev(bias, "bias", torch.float32), _dev(dy, "dy", x.dtype),
-                                      _dev(dx, "dx", x.dtype), _dev(dz, "dz", x.dtype),
-                                      _dev(dU, "dU", torch.float32), _dev(db, "db", torch.float32), B, T, D, W, R,
-                                      _dt(x), cu, n, _stream(stream))
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_lowrank_bwd_noalloc(_dev(x, "x"), _dev(z, "z", x.dtype, device=dev),
+                                      _dev(U, "U", x.dtype, device=dev), _dev(bias, "bias", torch.float32, device=dev),
+                                      _dev(dy, "dy", x.dtype, x.shape, dev), _dev(dx, "dx", x.dtype, x.shape, dev),
+                                      _dev(dz, "dz", x.dtype, z.shape, dev),
+                                      _dev(dU, "dU", torch.float32, U.shape, dev),
+                                      _dev(db, "db", torch.float32, bias.shape, dev), B, T, D, W, R, _dt(x), cu, n,
+                                      _stream(stream))
     _check(s, "dsc_lowrank_bwd_noalloc")
     return dx, dz, dU, db
 
 
 def dsc_static_fwd(x, w, y=None, *, cu_seqlens=None, stream=None):
     """Static short convolution: x [B,T,D], w [D,W] (one filter for every token); returns y [B,T,D]."""
+    dev = _lead(x, "x", 3)
     B, T, D = x.shape
     if w.dim() != 2 or w.shape[0] != D:
         raise ValueError("shapes: x [B,T,D]; w [D,W]")
     W = w.shape[1]
     y = torch.empty_like(x) if y is None else y
-    cu, n = _cu(cu_seqlens)
-    s = lib().dsc_static_fwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(y, "y", x.dtype), B, T, D, W, _dt(x), cu, n,
-                             _stream(stream))
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_static_fwd(_dev(x, "x"), _dev(w, "w", x.dtype, device=dev), _dev(y, "y", x.dtype, x.shape, dev),
+                             B, T, D, W, _dt(x), cu, n, _stream(stream))
     _check(s, "dsc_static_fwd")
     return y
 
 
 def dsc_static_bwd(x, w, dy, dx=None, dw=None, *, cu_seqlens=None, stream=None):
     """(dx [B,T,D], dw [D,W] fp32) of the static convolution for the upstream gradient dy."""
+    dev = _lead(x, "x", 3)
     B, T, D = x.shape
-    if w.dim() != 2 or w.shape[0] != D or tuple(dy.shape) != (B, T, D):
+    if w.dim() != 2 or w.shape[0] != D:
         raise ValueError("shapes: x, dy [B,T,D]; w [D,W]")
     W = w.shape[1]
     dx = torch.empty_like(x) if dx is None else dx
     dw = torch.empty((D, W), dtype=torch.float32, device=x.device) if dw is None else dw
-    cu, n = _cu(cu_seqlens)
-    s = lib().dsc_static_bwd(_dev(x, "x"), _dev(w, "w", x.dtype), _dev(dy, "dy", x.dtype), _dev(dx, "dx", x.dtype),
-                             _dev(dw, "dw", torch.float32), B, T, D, W, _dt(x), cu, n, _stream(stream))
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_static_bwd(_dev(x, "x"), _dev(w, "w", x.dtype, device=dev), _dev(dy, "dy", x.dtype, x.shape, dev),
+                             _dev(dx, "dx", x.dtype, x.shape, dev), _dev(dw, "dw", torch.float32, (D, W), dev), B, T,
+                             D, W, _dt(x), cu, n, _stream(stream))
     _check(s, "dsc_static_bwd")
     return dx, dw
 
@@ -239,6 +282,7 @@ def dsc_static_bwd(x, w, dy, dx=None, dw=None, *, cu_seqlens=None, stream=None):
 def dsc_decode_step(x, w, hist, pos, y=None, *, stream=None):
     """One decode step for B sequences: x [B,D], w [B,D/H,W], hist [B,W-1,D] (ring, updated in place),
     pos [B] int32 (document positions, read only); returns y [B,D]."""
+    dev = _lead(x, "x", 2)
     B, D = x.shape
     if w.dim() != 3 or w.shape[0] != B or w.shape[1] < 1 or D % w.shape[1]:
         raise ValueError("shapes: x [B,D]; w [B,D/H,W]")
@@ -246,15 +290,16 @@ def dsc_decode_step(x, w, hist, pos, y=None, *, stream=None):
     if tuple(hist.shape) != (B, W - 1, D) or tuple(pos.shape) != (B,):
         raise ValueError("shapes: hist [B,W-1,D]; pos [B]")
     y = torch.empty_like(x) if y is None else y
-    hp = _dev(hist, "hist", x.dtype) if W > 1 else None
-    s = lib().dsc_decode_step(_dev(x, "x"), _dev(w, "w", x.dtype), hp, _dev(pos, "pos", torch.int32),
-                              _dev(y, "y", x.dtype), B, D, W, D // w.shape[1], _dt(x), _stream(stream))
+    hp = _dev(hist, "hist", x.dtype, device=dev) if W > 1 else None
+    s = lib().dsc_decode_step(_dev(x, "x"), _dev(w, "w", x.dtype, device=dev), hp,
+                              _dev(pos, "pos", torch.int32, device=dev), _dev(y, "y", x.dtype, x.shape, dev), B, D, W,
+                              D // w.shape[1], _dt(x), _stream(stream))
     _check(s, "dsc_decode_step")
     return y
 
 
 def dsc_validate_cu_seqlens(cu_seqlens, B, T, *, stream=None) -> None:
-    cu, n = _cu(cu_seqlens)
+    cu, n = _cu(cu_seqlens, _lead(cu_seqlens, "cu_seqlens", 1))
     _check(lib().dsc_validate_cu_seqlens(cu, n, B, T, _stream(stream)), "dsc_validate_cu_seqlens")
 
 

@@ -69,6 +69,21 @@ def test_header_compiles_as_c_and_links(L, tmp_path):
     assert r.returncode == 0 and "DSC_ERR_INVALID_ARG" in r.stdout, r.stdout + r.stderr
 
 
+def test_binding_refuses_host_tensors():
+    """The Python entry points take CUDA tensors only; host tensors are refused before the library is used."""
+    import torch
+
+    import dynamic_short_convolution_gb300 as dsc
+
+    x = torch.zeros(1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        dsc.dsc_fwd(x, torch.zeros(1, 8, 4, 4, dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        dsc.dsc_static_fwd(x, torch.zeros(64, 4, dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        dsc.dsc_decode_step(x[0], torch.zeros(8, 4, 4, dtype=torch.bfloat16), None, None)
+
+
 def test_status_strings(L):
     assert L.dsc_status_string(0) == b"DSC_OK"
     assert L.dsc_status_string(4) == b"DSC_ERR_TIMEOUT"
