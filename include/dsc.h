@@ -224,7 +224,9 @@ dsc_status dsc_validate_cu_seqlens(const int32_t *cu_seqlens, int n_docs, int B,
  * dsc_sync_status -- synchronise `stream`, then read and clear the device
  * status word of the current device.  Returns DSC_OK, DSC_ERR_TIMEOUT (a
  * kernel's bounded wait gave up), DSC_ERR_INVALID_ARG (a failed
- * dsc_validate_cu_seqlens) or DSC_ERR_CUDA.
+ * dsc_validate_cu_seqlens, or a negative position given to dsc_decode_step)
+ * or DSC_ERR_CUDA.  The word is shared by every stream of the device: with
+ * calls in flight on several streams, a status may come from any of them.
  */
 dsc_status dsc_sync_status(cudaStream_t stream);
 
