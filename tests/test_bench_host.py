@@ -48,3 +48,10 @@ def test_whole_job_throughput_counts_every_replica():
     # 4 replicas of 16384 tokens, 10 steps in 2 ms of the slowest rank's time
     assert abs(bench.whole_job_tokens_per_s(4, 16384, 10, 2.0) - 4 * 16384 * 10 / 2e-3) < 1e-6
     assert bench.max_over_ranks(3.5, 1, None) == 3.5
+
+
+def test_peaks_fall_back_to_the_stated_figures_without_the_measured_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks() == (6800.0, 1900.0, 1700.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6783.1, "bf16_tflops": 1883.2}')
+    assert bench.peaks() == (6783.1, 1883.2, 1883.2, "measured")
