@@ -3,12 +3,15 @@
 
 Metric: fwd+bwd tokens/s and achieved HBM GB/s (fraction of the measured HBM
 roofline).  One step = one forward (dsc_fwd) and one backward (dsc_bwd) pass
-over one batch of the head-wise bf16 workload (B=8, T=2048, D=2048, W=4,
-H=16: Q/K/V-sized activations at about 2B-model width, the shape on which the
-pages quote their head-wise kernel) with inputs resident in HBM.  Steps run
-back to back and rotate over independent copies of the workload's tensors
-(at least 600 MB together, several times the 129 MB L2), so every step reads
-inputs that are not in L2 and each kernel pays for its own write-backs.
+over one batch of the largest single-GPU workload, the Q/K/V placement over
+packed documents (B=4, T=8192, D=3072 = Q, K and V of a 2048-wide model side by
+side, W=4, head size H=16, document lengths ~U{128..4096}), with inputs
+resident in HBM.  Steps run back to back and rotate over independent copies
+of the workload's tensors (at least 600 MB together, several times the 129 MB
+L2), so every step reads inputs that are not in L2 and each kernel pays for
+its own write-backs.  Every other workload (head-wise, materialised,
+low-rank, static, decode) is timed the same way in the ``rows`` table, each
+with its own roofline fraction and its own CPU-oracle baseline.
 
 Prints ONE JSON line on rank 0.  Multi-GPU (torchrun) runs one independent
 replica per GPU ("weak" scaling; the path shards by batch with no exchange).
@@ -35,7 +38,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "dyn-conv fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 roofline)"
 UNIT = "tokens/s"
-MAIN_WORKLOAD = "headwise_bf16"
+MAIN_WORKLOAD = "qkv_packed_bf16"
 ROTATE_BYTES = 600 << 20  # minimum bytes across the rotating copies
 
 
@@ -469,6 +472,9 @@ def oracle_tokens_per_s(wl, budget_s, min_tokens=64):
 
 
 def _oracle_step(oracle, wl, d, r0, r1):
+    """One fwd + bwd sample of the oracle: every per-token output over tokens [r0, r1), and, for the
+    low-rank form, its parameter gradients dU and db (sums over every token) over the same fraction of
+    their filter columns, so each output's share of the work matches the sample's share of the tokens."""
     if wl.kind == "static":
         oracle.static_fwd(d["x"], d["w"], wl.W, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
         oracle.static_bwd(d["x"], d["w"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"], rows=(r0, r1), want_dw=False)
@@ -476,9 +482,46 @@ def _oracle_step(oracle, wl, d, r0, r1):
         oracle.lowrank_fwd(d["x"], d["z"], d["U"], d["bias"], wl.W, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
         oracle.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
                            rows=(r0, r1), want=("dx", "dz"))
+        nw, BT = wl.D * wl.W, wl.B * wl.T
+        c0 = (r0 * nw) // BT
+        c1 = max(c0 + 1, (r1 * nw) // BT)
+        oracle.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
+                           cols=list(range(c0, min(c1, nw))), want=("dU", "db"))
+    elif wl.kind == "decode":  # one decode step of sequences [r0, r1) (no backward: inference)
+        oracle.decode_step(d["x"][r0:r1], d["w"][r0:r1], d["hist"][r0:r1], d["pos"][r0:r1], wl.W, wl.H)
     else:
         oracle.fwd(d["x"], d["w"], wl.W, wl.H, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
         oracle.bwd(d["x"], d["w"], d["dy"], wl.W, wl.H, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
+
+
+def _omp_threads(n):
+    """Set the OpenMP thread count of the oracle's parallel loops (the calling thread's setting)."""
+    import ctypes
+
+    try:
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(int(n))
+        return True
+    except OSError:
+        return False
+
+
+def cpu_rows(budget_s=2.5):
+    """The oracle, as it stands, on a bounded sample of every workload (tokens/s on the host cores), and
+    the tiny fp32 workload also on one thread.  Run before any GPU work."""
+    from dynamic_short_convolution_gb300 import inputs
+
+    out = {}
+    cores = host_cores()
+    for wl in inputs.WORKLOADS.values():
+        v, n, spent = oracle_tokens_per_s(wl, budget_s=budget_s)
+        r = {"cpu_tokens_per_s": v, "cpu_cores": cores,
+             "cpu_sample": f"{n} tokens of {wl.name} in {spent:.1f} s" + ("" if wl.kind == "decode" else ", fwd + bwd")}
+        if wl.wid == 1 and _omp_threads(1):
+            v1, n1, s1 = oracle_tokens_per_s(wl, budget_s=budget_s)
+            _omp_threads(cores)
+            r.update({"cpu_tokens_per_s_1thread": v1, "cpu_sample_1thread": f"{n1} tokens in {s1:.1f} s on one thread"})
+        out[wl.name] = r
+    return out
 
 
 def host_cores():
@@ -583,6 +626,7 @@ def main():
         cpu = {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                "sample": f"{n} tokens (all {wl.D} channels; consecutive ranges of {wl.name}, wrapping) fwd + bwd "
                          f"in {spent:.1f} s"}
+    crows = cpu_rows() if rank == 0 and world == 1 and not args.no_cpu and not args.no_rows else None
 
     import torch
     import torch.distributed as dist
@@ -661,8 +705,23 @@ def main():
     rows = None
     if rank == 0 and world == 1 and not args.no_rows:
         rows = measure_rows(dev, hbm_peak, tc_peak)
+        for name, r in (crows or {}).items():
+            if name in rows:
+                rows[name].update(r)
 
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if clocks is not None and clocks.get("samples_in_timed_region", 0) < 3:
+        # the timed region was shorter than a few sampling periods: run the same steps again, untimed, for
+        # about a second, and report the clocks seen there beside it
+        chk = ClockSampler(dev.index)
+        chk.start()
+        c0 = time.perf_counter()
+        while time.perf_counter() - c0 < 1.2:
+            time_steps(prob, max(1, min(args.steps, 200)))
+        torch.cuda.synchronize()
+        c1 = time.perf_counter()
+        chk.stop()
+        clocks["same_steps_for_1s_after"] = chk.summary(c0, c1)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -12,12 +12,13 @@
 namespace dsc {
 
 // One status word per device (static device memory: no allocation).  Kernels
-// record the first error of any launch here; dsc_sync_status reads and clears.
+// record the first error of any launch here; dsc_sync_status takes it (reads
+// and clears it in one atomic exchange) into g_status_taken.
 __device__ int g_status_word;
+__device__ int g_status_taken;
 
 static std::mutex g_mu;
 static constexpr int kMaxDevices = 64;
-static int *g_status_ptr[kMaxDevices] = {};
 static DeviceInfo g_dev[kMaxDevices] = {};
 static bool g_dev_ok[kMaxDevices] = {};
 static std::atomic<unsigned long long> g_wait_ns{1000000000ull};  // about one second
@@ -25,18 +26,47 @@ static std::atomic<unsigned long long> g_launches{0};
 
 void count_launch(unsigned n) { g_launches.fetch_add(n); }
 
-int *device_status_word()
+// cuCtxGetCurrent through the runtime's driver entry point (no libcuda link).
+using PfnCtxGetCurrent = CUresult (*)(CUcontext *);
+static PfnCtxGetCurrent ctx_get_current_fn()
+{
+    static PfnCtxGetCurrent fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PfnCtxGetCurrent>(p);
+    });
+    return fn;
+}
+
+static CUcontext current_context()
+{
+    CUcontext c = nullptr;
+    auto fn = ctx_get_current_fn();
+    if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+    return c;
+}
+
+void *symbol_address(SymbolCache *cache, const void *symbol)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_status_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-        g_status_ptr[dev] = static_cast<int *>(p);
-    }
-    return g_status_ptr[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SymbolCache::kDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(cache->mu);
+    const CUcontext cur = current_context();
+    if (cache->addr[dev] && cur != nullptr && cache->ctx[dev] == cur) return cache->addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+    cache->ctx[dev] = current_context();  // the runtime call above made the device's context current
+    cache->addr[dev] = p;
+    return p;
 }
+
+static SymbolCache g_status_cache, g_taken_cache;
+
+int *device_status_word() { return static_cast<int *>(symbol_address(&g_status_cache, &g_status_word)); }
 
 unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
 
@@ -103,6 +133,10 @@ __global__ void validate_cu_kernel(const int32_t *cu, int n_docs, long long BT, 
     }
     if (bad) record_status(status, kStatusInvalid);
 }
+
+// Read and clear the status word in one atomic step, so an error that a kernel on
+// another stream records meanwhile is never lost.
+__global__ void take_status_kernel(int *st, int *taken) { *taken = atomicExch(st, 0); }
 
 // A wait on an mbarrier that nothing ever arrives at: exercises the bounded
 // wait and the timeout status without hanging anything.
@@ -300,11 +334,13 @@ dsc_status dsc_sync_status(cudaStream_t stream)
 {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return DSC_ERR_CUDA;
     int *st = device_status_word();
-    if (!st) return DSC_ERR_CUDA;
+    int *taken = static_cast<int *>(symbol_address(&g_taken_cache, &g_status_taken));
+    if (!st || !taken) return DSC_ERR_CUDA;
+    take_status_kernel<<<1, 1, 0, stream>>>(st, taken);
+    if (cudaGetLastError() != cudaSuccess) return DSC_ERR_CUDA;
     int v = 0;
-    if (cudaMemcpy(&v, st, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return DSC_ERR_CUDA;
-    const int zero = 0;
-    if (v != 0 && cudaMemcpy(st, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return DSC_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, taken, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return DSC_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DSC_ERR_CUDA;
     return static_cast<dsc_status>(v);
 }
 

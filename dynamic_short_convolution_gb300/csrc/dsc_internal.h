@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "dsc.h"
@@ -77,6 +78,16 @@ size_t lowrank_bwd_workspace(int B, int T, int D, int W, int R);
 dsc_status static_fwd(const StaticArgs &a);
 dsc_status static_bwd(const StaticArgs &a);
 dsc_status decode_step(const DecodeArgs &a);
+
+// Device address of a file-scope __device__ variable on the current device, looked up once per device
+// and context (looked up again after the context changes, e.g. after cudaDeviceReset).
+struct SymbolCache {
+    static constexpr int kDevices = 64;
+    std::mutex mu;
+    CUcontext ctx[kDevices] = {};
+    void *addr[kDevices] = {};
+};
+void *symbol_address(SymbolCache *cache, const void *symbol);
 
 // Per-device status word (device address) and the current wait limit.
 int *device_status_word();

@@ -31,8 +31,6 @@
 // Row exchange for dx: the tap-k term of token t lands on token t-k, which is
 // another TMEM lane: warp shuffles inside a warp, a small shared edge buffer
 // across the four lane quadrants.
-#include <mutex>
-
 #include "dsc_internal.h"
 #include "dsc_tcgen05.cuh"
 
@@ -818,21 +816,9 @@ constexpr size_t kNoAllocScratchFloats = size_t(1) << 21;  // 8 MiB: B*T*R <= 2,
 static __device__ __align__(256) float g_lrb_scratch[kNoAllocScratchFloats];
 
 // Device address of g_lrb_scratch on the current device, looked up once per
-// device (host code may not use the symbol itself as an address).
-static float *noalloc_scratch()
-{
-    static std::mutex mu;
-    static float *addr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_lrb_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<float *>(ptr);
-    }
-    return addr[dev];
-}
+// device and context (host code may not use the symbol itself as an address).
+static SymbolCache g_scratch_cache;
+static float *noalloc_scratch() { return static_cast<float *>(symbol_address(&g_scratch_cache, &g_lrb_scratch)); }
 
 }  // namespace dsc
 

@@ -2,6 +2,7 @@
 for callers that cannot allocate device memory for a workspace: its results
 must match the regular entry point's on two calls in a row.  Collected last
 (file name) so that a failure here comes after every other test has run."""
+import numpy as np
 import pytest
 import torch
 
@@ -33,14 +34,47 @@ def test_noalloc_matches_regular_entry_point_twice():
             assert_close(a, b.double().cpu().numpy(), "bf16", f"noalloc {name}")
 
 
+def test_noalloc_at_its_size_limit_against_the_oracle(oracle_mod):
+    """B*T*R exactly at the limit (the last fp32 value of the static array in use), checked against the
+    oracle: dx and dz on sampled token windows (start, end, across sequence and document starts), dU and
+    db on sampled filter columns."""
+    import dynamic_short_convolution_gb300 as dsc
+
+    wl = inputs.custom(1, 32768, 256, 4, R=64, dtype="bf16", seed_id=883, packed=True, doc_min=100, doc_max=5000)
+    assert wl.B * wl.T * wl.R == 2 ** 21
+    d = inputs.make(wl)
+    g = _dev(d)
+    dx, dz, dU, db = dsc.dsc_lowrank_bwd_noalloc(g["x"], g["z"], g["U"], g["bias"], g["dy"],
+                                                 cu_seqlens=g["cu_seqlens"])
+    assert dsc.dsc_sync_status() == dsc.DSC_OK
+    BT = wl.B * wl.T
+    dx, dz = dx.reshape(BT, wl.D), dz.reshape(BT, wl.R)
+    cu = d["cu_seqlens"].tolist()
+    rng = np.random.default_rng(883)
+    starts = sorted({0, BT - 6, cu[1] - 3, cu[len(cu) // 2] - 2, *map(int, rng.integers(0, BT - 6, size=4))})
+    for r0 in starts:
+        r1 = min(r0 + 6, BT)
+        ref = oracle_mod.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
+                                     rows=(r0, r1), want=("dx", "dz"))
+        assert_close(dx[r0:r1], ref["dx"], "bf16", f"noalloc dx rows {r0}:{r1}")
+        assert_close(dz[r0:r1], ref["dz"], "bf16", f"noalloc dz rows {r0}:{r1}")
+    nw = wl.D * wl.W
+    cols = sorted({0, 1, 2, 3, nw - 1, nw - 4, *map(int, rng.integers(0, nw, size=26))})
+    ref = oracle_mod.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
+                                 cols=cols, want=("dU", "db"))
+    assert_close(dU[:, cols], ref["dU"], "bf16", "noalloc dU columns")
+    assert_close(db[cols], ref["db"], "bf16", "noalloc db columns")
+
+
 def test_noalloc_rejects_sizes_beyond_its_array():
     import dynamic_short_convolution_gb300 as dsc
 
-    B, T, D, W, R = 1, 40000, 64, 4, 64  # B*T*R = 2,560,000 > 2,097,152
-    x = torch.zeros(B, T, D, dtype=torch.bfloat16, device=DEV)
-    z = torch.zeros(B, T, R, dtype=torch.bfloat16, device=DEV)
-    U = torch.zeros(R, D * W, dtype=torch.bfloat16, device=DEV)
-    b = torch.zeros(D * W, dtype=torch.float32, device=DEV)
-    with pytest.raises(dsc.DscError) as e:
-        dsc.dsc_lowrank_bwd_noalloc(x, z, U, b, x)
-    assert e.value.status == dsc.DSC_ERR_INVALID_ARG
+    for T in (32769, 40000):  # B*T*R = 2,097,216 (one token over the limit) and 2,560,000
+        B, D, W, R = 1, 64, 4, 64
+        x = torch.zeros(B, T, D, dtype=torch.bfloat16, device=DEV)
+        z = torch.zeros(B, T, R, dtype=torch.bfloat16, device=DEV)
+        U = torch.zeros(R, D * W, dtype=torch.bfloat16, device=DEV)
+        b = torch.zeros(D * W, dtype=torch.float32, device=DEV)
+        with pytest.raises(dsc.DscError) as e:
+            dsc.dsc_lowrank_bwd_noalloc(x, z, U, b, x)
+        assert e.value.status == dsc.DSC_ERR_INVALID_ARG
