@@ -77,12 +77,13 @@ def kernel_source_digest(files):
 
 DENSE_BWD_SRC = ["dsc_dense_bwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 DENSE_FWD_SRC = ["dsc_dense_fwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
-LOWRANK_BWD_SRC = ["dsc_lowrank_bwd.cu", "dsc_tcgen05.cuh", "dsc_device.cuh"]
+LOWRANK_BWD_SRC = ["dsc_lowrank_bwd.cu", "dsc_lowrank_bwd_du.cu", "dsc_lowrank_common.cuh", "dsc_tcgen05.cuh",
+                   "dsc_device.cuh"]
 LOWRANK_FWD_SRC = ["dsc_lowrank_fwd.cu", "dsc_tcgen05.cuh", "dsc_device.cuh"]
 STATIC_SRC = ["dsc_static.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 # (kernel name in the ncu launch list, source files) per workload kind and direction
 KERNELS = {("dense", "bwd"): ("dense_bwd_tma", DENSE_BWD_SRC), ("dense", "fwd"): ("dense_fwd_tma", DENSE_FWD_SRC),
-           ("lowrank", "bwd"): ("lowrank_bwd_tc", LOWRANK_BWD_SRC),
+           ("lowrank", "bwd"): ("lowrank_bwd_dxdz+lowrank_bwd_dudb", LOWRANK_BWD_SRC),
            ("lowrank", "fwd"): ("lowrank_fwd_tc", LOWRANK_FWD_SRC),
            ("static", "bwd"): ("static_bwd_tma", STATIC_SRC), ("static", "fwd"): ("static_fwd_tma", STATIC_SRC)}
 

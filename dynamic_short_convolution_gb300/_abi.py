@@ -227,9 +227,9 @@ def dsc_lowrank_bwd(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=None, works
 
 def dsc_lowrank_bwd_noalloc(x, z, U, bias, dy, dx=None, dz=None, dU=None, db=None, *, cu_seqlens=None,
                             stream=None):
-    """dsc_lowrank_bwd without a caller workspace, for callers that cannot allocate device memory for one:
-    the library's own fixed 8 MiB device array holds the partial sums (B*T*R <= 2,097,152; calls that
-    overlap on the GPU race on it).  The output tensors, when not given, are allocated here by torch."""
+    """dsc_lowrank_bwd through the entry point that takes no workspace, for callers that cannot
+    allocate device memory: the library keeps a fixed 2 MiB device array for the bias rows, which limits
+    D*W + 256 to 131072.  The output tensors, when not given, are allocated here by torch."""
     dev, (B, T, D, W, R) = _lowrank_dims(x, z, U, bias)
     dx = torch.empty_like(x) if dx is None else dx
     dz = torch.empty_like(z) if dz is None else dz

@@ -226,7 +226,7 @@ static dsc_status lowrank_check(const void *x, const void *z, const void *U, con
     if (!dims_ok(B, T, D, W) || R < 1 || !cu_ok(cu, n_docs)) return DSC_ERR_INVALID_ARG;
     if (!x || !z || !U || !bias) return DSC_ERR_INVALID_ARG;
     if (dt == DSC_F32) return DSC_ERR_UNSUPPORTED;
-    if (D % 8 != 0 || R % 8 != 0 || R > 128) return DSC_ERR_UNSUPPORTED;
+    if (D % 8 != 0 || R % 8 != 0 || R > 256) return DSC_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(z) || !aligned16(U) || !aligned16(bias)) return DSC_ERR_UNSUPPORTED;
     if (static_cast<long long>(D) * W * R >= (1LL << 31) || static_cast<long long>(B) * T * R >= (1LL << 31))
         return DSC_ERR_INVALID_ARG;
@@ -254,16 +254,29 @@ size_t dsc_lowrank_bwd_workspace_bytes(int B, int T, int D, int W, int R)
     return lowrank_bwd_workspace(B, T, D, W, R);
 }
 
+}  // extern "C"
+
+// The backward's checks of everything but the workspace (shared with the allocation-free entry point).
+dsc_status dsc::lowrank_bwd_validate(const void *x, const void *z, const void *U, const float *bias, const void *dy,
+                                     void *dx, void *dz, float *dU, float *db, int B, int T, int D, int W, int R,
+                                     dsc_dtype dt, const int32_t *cu_seqlens, int n_docs)
+{
+    dsc_status s = lowrank_check(x, z, U, bias, B, T, D, W, R, dt, cu_seqlens, n_docs);
+    if (s != DSC_OK) return s;
+    if (!dy || !dx || !dz || !dU || !db) return DSC_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(dx) || !aligned16(dz) || !aligned16(dU) || !aligned16(db))
+        return DSC_ERR_UNSUPPORTED;
+    return DSC_OK;
+}
+
+extern "C" {
+
 dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const float *bias, const void *dy, void *dx,
                            void *dz, float *dU, float *db, void *workspace, int B, int T, int D, int W, int R,
                            dsc_dtype dt, const int32_t *cu_seqlens, int n_docs, cudaStream_t stream)
 {
-    dsc_status s = lowrank_check(x, z, U, bias, B, T, D, W, R, dt, cu_seqlens, n_docs);
+    dsc_status s = lowrank_bwd_validate(x, z, U, bias, dy, dx, dz, dU, db, B, T, D, W, R, dt, cu_seqlens, n_docs);
     if (s != DSC_OK) return s;
-    if (R % 16 != 0 || R > 64) return DSC_ERR_UNSUPPORTED;  // the backward's TMEM plan: dz is R <= 64 columns
-    if (!dy || !dx || !dz || !dU || !db) return DSC_ERR_INVALID_ARG;
-    if (!aligned16(dy) || !aligned16(dx) || !aligned16(dz) || !aligned16(dU) || !aligned16(db))
-        return DSC_ERR_UNSUPPORTED;
     const size_t ws = lowrank_bwd_workspace(B, T, D, W, R);
     if (ws > 0 && (workspace == nullptr || (reinterpret_cast<unsigned long long>(workspace) & 255ull) != 0))
         return DSC_ERR_INVALID_ARG;

@@ -75,6 +75,11 @@ dsc_status dense_bwd(const DenseArgs &a);
 dsc_status lowrank_fwd(const LowrankArgs &a);
 dsc_status lowrank_bwd(const LowrankArgs &a);
 size_t lowrank_bwd_workspace(int B, int T, int D, int W, int R);
+dsc_status lowrank_bwd_validate(const void *x, const void *z, const void *U, const float *bias, const void *dy, void *dx,
+                                void *dz, float *dU, float *db, int B, int T, int D, int W, int R, dsc_dtype dt,
+                                const int32_t *cu_seqlens, int n_docs);
+struct DeviceInfo;
+dsc_status lowrank_bwd_dudb(const LowrankArgs &a, const DeviceInfo &dev);  // second kernel of lowrank_bwd
 dsc_status static_fwd(const StaticArgs &a);
 dsc_status static_bwd(const StaticArgs &a);
 dsc_status decode_step(const DecodeArgs &a);

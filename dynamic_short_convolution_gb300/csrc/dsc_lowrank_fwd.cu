@@ -456,6 +456,7 @@ dsc_status lowrank_fwd(const LowrankArgs &a)
 {
     DeviceInfo dev;
     if (!device_info(&dev)) return DSC_ERR_CUDA;
+    if (a.R > 128) return DSC_ERR_UNSUPPORTED;
     switch (a.W) {
     case 1: return launch_lowrank_fwd<1, 64>(a, dev);
     case 2: return launch_lowrank_fwd<2, 64>(a, dev);

@@ -118,7 +118,9 @@ dsc_status dsc_lowrank_fwd(const void *x, const void *z, const void *U, const fl
 
 /*
  * Bytes of caller-provided device workspace dsc_lowrank_bwd needs for these
- * sizes (0 is a valid answer).  The workspace holds fp32 partial sums.
+ * sizes: 16 * (D*W + 256) rounded up to 256, independent of B, T and R.  The
+ * workspace holds the generator bias split into bf16 high and low halves,
+ * one 16-byte row per group of 8 filter entries, written by the call itself.
  */
 size_t dsc_lowrank_bwd_workspace_bytes(int B, int T, int D, int W, int R);
 
@@ -132,9 +134,11 @@ size_t dsc_lowrank_bwd_workspace_bytes(int B, int T, int D, int W, int R);
  *     db[n]   = sum_t G[t,n]               (fp32 [D*W])
  *   `workspace` must hold dsc_lowrank_bwd_workspace_bytes() bytes of device
  *   memory, 256-byte aligned (may be NULL when that size is 0); its contents on
- *   entry are ignored.  Same requirements as dsc_lowrank_fwd, and in addition
- *   R % 16 == 0 and R <= 64 (other ranks return DSC_ERR_UNSUPPORTED before
- *   anything is launched).
+ *   entry are ignored.  Same requirements as dsc_lowrank_fwd except the rank:
+ *   R % 8 == 0 and 8 <= R <= 256 (other ranks return DSC_ERR_UNSUPPORTED
+ *   before anything is launched).  dy, dx, dz, dU and db must be non-NULL and
+ *   16-byte aligned (else DSC_ERR_INVALID_ARG).  dx and dz are deterministic;
+ *   dU and db are sums of fp32 partials added in a run-dependent order.
  */
 dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const float *bias, const void *dy, void *dx,
                            void *dz, float *dU, float *db, void *workspace, int B, int T, int D, int W, int R,
@@ -146,18 +150,18 @@ dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const fl
  * memory pool under a fixed memory plan, or a latency-critical loop that must
  * never enter the allocator.  The paper has no counterpart; this is an
  * interface convenience.  Same arguments and results as dsc_lowrank_bwd,
- * without `workspace`: the fp32 partial sums go to a fixed array of 8 MiB in
- * the library's static device memory, held by every GPU that loads the
- * library until the process exits.  Nothing is allocated or freed by the
- * call, and no allocating library routine is used.
- *   Limit: B*T*R <= 2,097,152 (the array holds that many fp32 values);
+ * without `workspace`: the bias rows go to a fixed array of 2 MiB in the
+ * library's static device memory, held by every GPU that loads the library
+ * until the process exits.  Nothing is allocated or freed by the call, and no
+ * allocating library routine is used.
+ *   Limit: D*W + 256 <= 131,072 (the array holds that many 16-byte rows);
  *   larger sizes return DSC_ERR_INVALID_ARG before anything is launched.
  *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.
- *   Every call uses the same array and leaves its last contents there; the
- *   call clears what must start at zero itself.  Calls that overlap on the GPU
- *   (for example on two streams) race on the array: serialise them.
+ *   device and context, with that device current); make that first call
+ *   before any stream capture.
+ *   Every call uses the same array and rewrites it before reading it.  Calls
+ *   that overlap on the GPU (for example on two streams) race on the array:
+ *   serialise them.
  */
 dsc_status dsc_lowrank_bwd_noalloc(const void *x, const void *z, const void *U, const float *bias, const void *dy,
                                    void *dx, void *dz, float *dU, float *db, int B, int T, int D, int W, int R,

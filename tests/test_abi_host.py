@@ -106,12 +106,21 @@ def test_rejects_bad_arguments_before_any_launch(L):
     assert L.dsc_fwd(p, p, p, 1 << 16, 1 << 16, 8, 4, 1, bf16, None, 0, None) == 1  # int32 size limit
     # low-rank: fp32 unsupported, R out of range unsupported
     assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 16, f32, None, 0, None) == 2
-    assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 256, bf16, None, 0, None) == 2
+    # (every call below is rejected before any launch: the pointers are not device memory)
+    for r in (12, 264, 512):  # R a multiple of 8, at most 256
+        assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, r, bf16, None, 0, None) == 2
+        assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, r, bf16, None, 0, None) == 2
+        assert L.dsc_lowrank_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 8, 64, 4, r, bf16, None, 0, None) == 2
     assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 0, bf16, None, 0, None) == 1
-    # low-rank backward: R a multiple of 16 up to 64 only
-    for r in (8, 24, 80, 128):
-        assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, p, 1, 8, 64, 4, r, bf16, None, 0, None) == 2
-    assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, 16, bf16, None, 0, None) == 1  # no workspace
+    assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, 0, bf16, None, 0, None) == 1
+    assert L.dsc_lowrank_bwd(p, p, p, p, None, p, p, p, p, None, 1, 8, 64, 4, 16, bf16, None, 0, None) == 1  # no dy
+    # the backward's workspace: 16 bytes per filter column (the bias rows) and 256 rows of padding, whatever
+    # B, T and R; a null workspace is refused
+    for b, t, r in ((8, 2048, 8), (1, 5, 64), (8, 2048, 256)):
+        assert L.dsc_lowrank_bwd_workspace_bytes(b, t, 2048, 4, r) == 16 * (2048 * 4 + 256)
+    assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, 16, bf16, None, 0, None) == 1
+    # the allocation-free entry point holds at most D*W + 256 = 131072 rows in its array
+    assert L.dsc_lowrank_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 8, 32712, 4, 16, bf16, None, 0, None) == 1
     assert L.dsc_validate_cu_seqlens(None, 3, 1, 8, None) == 1
     # static convolution: the same size, W, dtype and alignment rules; dw must be fp32-aligned
     assert L.dsc_static_fwd(p, p, p, 0, 8, 64, 4, bf16, None, 0, None) == 1
