@@ -8,17 +8,23 @@
 // Work unit: one block of SCB channels (SNB = SCB*W filter columns) x one tile
 // of 128 tokens.  A persistent CTA walks a block-major run of units and keeps
 // the block's dU and db in TMEM over all of its tiles:
-//   epi  G = dy * x~ as an exact bf16 hi + lo pair (packed bf16 multiply and
-//        fused multiply-add), written 128-byte swizzled, tokens as rows
-//   MMA  [dU_hi | dU_lo] += [z^T; 1] . [G_hi | G_lo]   (A MN-major: the z tile,
-//        then an all-ones block whose rows give db; B MN-major; hi and lo side by
-//        side along N, so one MMA of N = 2*SNB reads A once for both)
-// At the end of a run the epilogue adds hi + lo and reduces them into dU and db
-// (fp32 additions: a block's tokens are split between at most a few CTAs).
-// dU and db are zeroed by the kernel launched just before this one
-// (lowrank_bwd_dxdz); every addition comes after the wait for it.  For R > 64
-// the z tile fills all 128 rows of A and db has an MMA of its own (A = ones);
-// for R > 128 dU takes two MMAs of 128 rows.
+//   epi  G = dy * x~ as an exact bf16 pair: -hi (the rounded product of the
+//        negated dy) and lo = dy * x~ - hi (one packed multiply and one fused
+//        multiply-add per two entries), with the W taps of each group of 8
+//        channels in tap-major order, so that an entry pair is the product of a
+//        dy word and an x word; written 128-byte swizzled, tokens as rows
+//   MMA  [acc_hi | acc_lo] += [z^T; 1] . [-G_hi | G_lo]  (A MN-major: the z
+//        tile, then an all-ones block whose rows give db; B MN-major; hi and lo
+//        side by side along N, so one MMA of N = 2*SNB reads A once for both)
+// At the end of a run the epilogue forms lo - (-hi) per accumulator column, puts
+// the columns back in the d*W + k order and reduces them into dU and db (fp32
+// additions: a block's tokens are split between at most a few CTAs).  CTAs work
+// in pairs on the two blocks of a block pair over the same token tiles, so the
+// two halves of every 128-byte row of x and dy are read together.  dU and db are
+// zeroed by the prep kernel two launches back; every addition comes after the
+// wait for the kernel before this one (which itself waited for the prep).  For
+// R > 64 the z tile fills all 128 rows of A and db has an MMA of its own
+// (A = ones); for R > 128 dU takes two MMAs of 128 rows.
 #include "dsc_internal.h"
 #include "dsc_lowrank_common.cuh"
 
@@ -38,7 +44,7 @@ struct Params {
     float *dU;
     float *db;
     int BT, T, D, R, N;
-    int n_mt, n_units, kchunks, rclass;
+    int n_mt, n_units, n_units_odd, kchunks, rclass;
     unsigned gbuf_bytes, z_off, z_bytes, xy_off, xy_bytes, dy_in, one_off;
     int nz, nxy, col_du1, col_db;
     int *status;
@@ -117,11 +123,20 @@ __global__ void __launch_bounds__(lrg::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     // the kernel before this one (lowrank_bwd_dxdz) let it launch after its own wait for the inputs, so the
-    // inputs may be read at once; dU and db (zeroed by that kernel) are touched only after grid_dependency_wait
+    // inputs may be read at once; dU and db (zeroed by the prep kernel before that one) are touched only after
+    // grid_dependency_wait
     const uint32_t tmem = hdr->tmem_base;
     volatile int *abort_flag = &hdr->abort_flag;
-    const int u_begin = static_cast<int>(static_cast<long long>(blockIdx.x) * p.n_units / gridDim.x);
-    const int u_end = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.n_units / gridDim.x);
+    // CTAs work in pairs: the two CTAs of a pair walk the same run of (block pair, token tile) units, the even
+    // one on the pair's first channel block, the odd one on its second, so the two 64-byte halves of the x and
+    // dy rows they read are fetched at about the same time.  Unit u of a CTA is block 2*(u / n_mt) + half.
+    const int half = static_cast<int>(blockIdx.x & 1u);
+    const long long pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    const int n_valid = half ? p.n_units_odd : p.n_units;  // an odd block count leaves the last pair one block
+    int u_end = static_cast<int>((pair + 1) * p.n_units / n_pairs);
+    u_end = u_end < n_valid ? u_end : n_valid;
+    int u_begin = static_cast<int>(pair * p.n_units / n_pairs);
+    u_begin = u_begin < u_end ? u_begin : u_end;
 
     int z_last[kMaxStages], xy_last[kMaxStages];  // last unit loaded into each slot (producer)
 #pragma unroll
@@ -134,7 +149,7 @@ __global__ void __launch_bounds__(lrg::kThreads, 1)
         uint32_t zph = 0, xph = 0;
         bool ok = true;
         for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
-            const int nb = u / p.n_mt, t0 = (u - nb * p.n_mt) * kM;
+            const int bp = u / p.n_mt, nb = 2 * bp + half, t0 = (u - bp * p.n_mt) * kM;
             if (i >= p.nxy) ok = warp_wait(&hdr->xy_empty[xs], xph ^ 1, p.wait_ns);
             ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
             if (!ok) break;
@@ -242,7 +257,7 @@ __global__ void __launch_bounds__(lrg::kThreads, 1)
             for (int kk = 0; kk < W; ++kk) off_x[gi][kk] = swzt<RB>(row + (W - 1) - kk, cw * GPW + gi);
         }
         for (int u = u_begin, i = 0; u < u_end && ok; ++u, ++i) {
-            const int nb = u / p.n_mt, mt = u - nb * p.n_mt;
+            const int bp = u / p.n_mt, nb = 2 * bp + half, mt = u - bp * p.n_mt;
             const bool first = (u == u_begin) || mt == 0, last = (u + 1 == u_end) || (mt + 1 == p.n_mt);
             const int cs = s;
             const uint32_t cph = ph;
@@ -279,19 +294,21 @@ __global__ void __launch_bounds__(lrg::kThreads, 1)
                         for (int kk = 1; kk < W; ++kk)
                             if (kk >= nv) xv[gi][kk] = make_uint4(0u, 0u, 0u, 0u);
                 }
+                // G per tap and channel pair, tap-major within the group (word kk*4 + e: channels 2e, 2e+1 of
+                // tap kk): -hi = the rounded product of the negated dy, lo = dy * x~ - hi (exact)
                 uint32_t ghi[GPW][4 * W], glo[GPW][4 * W];
 #pragma unroll
-                for (int gi = 0; gi < GPW; ++gi) {
+                for (int gi = 0; gi < GPW; ++gi)
 #pragma unroll
-                    for (int pr = 0; pr < 4 * W; ++pr) {
-                        const int f = 2 * pr;
-                        const int c0 = f / W, k0 = f % W, c1 = (f + 1) / W, k1 = (f + 1) % W;
-                        const uint32_t sel = half_sel(c0 & 1, c1 & 1);
-                        const uint32_t d2 = __byte_perm(word_of(dyv[gi], c0 >> 1), word_of(dyv[gi], c1 >> 1), sel);
-                        const uint32_t x2 = __byte_perm(word_of(xv[gi][k0], c0 >> 1), word_of(xv[gi][k1], c1 >> 1), sel);
-                        exact_product_split(d2, x2, ghi[gi][pr], glo[gi][pr]);
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t d = word_of(dyv[gi], e), nd = d ^ 0x80008000u;
+#pragma unroll
+                        for (int kk = 0; kk < W; ++kk) {
+                            const uint32_t xw = word_of(xv[gi][kk], e);
+                            ghi[gi][kk * 4 + e] = bmul2(nd, xw);
+                            glo[gi][kk * 4 + e] = bfma2(d, xw, ghi[gi][kk * 4 + e]);
+                        }
                     }
-                }
                 const int gb = i & 1;
                 w = i < 2 || warp_wait(&hdr->g_empty[gb], ((i >> 1) & 1) ^ 1, p.wait_ns);
                 w = __all_sync(0xffffffffu, w);
@@ -330,39 +347,41 @@ __global__ void __launch_bounds__(lrg::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                for (int c4 = cw; c4 < SNB / 4; c4 += 4) {
-                    const int n = nb * SNB + c4 * 4;
-                    uint32_t h[4], l[4];
-                    tmem_ld_x4(lane_base + c4 * 4, h);
-                    tmem_ld_x4(lane_base + SNBP + c4 * 4, l);
-                    float v[4];
-                    if (p.rclass == 2) {
-                        uint32_t h1[4], l1[4];
-                        tmem_ld_x4(lane_base + p.col_du1 + c4 * 4, h1);
-                        tmem_ld_x4(lane_base + p.col_du1 + SNBP + c4 * 4, l1);
-                        tmem_ld_wait();
+                // accumulator column g*8W + kk*8 + c (tap-major) is filter column (g*8 + c)*W + kk of the block;
+                // the high half was accumulated negated
+                for (int g = cw; g < GPS; g += 4) {
+                    const int n0 = nb * SNB + g * 8 * W;  // first filter column of the group
+                    auto flush_rows = [&](uint32_t col_acc, float *dst_row, bool on) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(h1[e]) + __uint_as_float(l1[e]);
-                        if (n < p.N && 128 + row < p.R)
-                            red_add_f4(p.dU + static_cast<size_t>(128 + row) * p.N + n, v[0], v[1], v[2], v[3]);
-                    }
-                    tmem_ld_wait();
+                        for (int hh = 0; hh < 2; ++hh) {  // channels 4hh .. 4hh+3 of the group
+                            uint32_t h[4 * W], l[4 * W];  // [kk*4 + e]: tap kk of channel 4hh + e
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(h[e]) + __uint_as_float(l[e]);
-                    if (n < p.N) {
-                        if (row < p.R && (p.rclass > 0 || row < 64))
-                            red_add_f4(p.dU + static_cast<size_t>(row) * p.N + n, v[0], v[1], v[2], v[3]);
-                        if (p.rclass == 0 && row == 64) red_add_f4(p.db + n, v[0], v[1], v[2], v[3]);
-                    }
-                    if (p.rclass > 0) {
-                        tmem_ld_x4(lane_base + p.col_db + c4 * 4, h);
-                        tmem_ld_x4(lane_base + p.col_db + SNBP + c4 * 4, l);
-                        tmem_ld_wait();
-                        if (n < p.N && row == 0)
-                            red_add_f4(p.db + n, __uint_as_float(h[0]) + __uint_as_float(l[0]),
-                                       __uint_as_float(h[1]) + __uint_as_float(l[1]),
-                                       __uint_as_float(h[2]) + __uint_as_float(l[2]),
-                                       __uint_as_float(h[3]) + __uint_as_float(l[3]));
+                            for (int kk = 0; kk < W; ++kk) {
+                                tmem_ld_x4(lane_base + col_acc + g * 8 * W + kk * 8 + 4 * hh, h + kk * 4);
+                                tmem_ld_x4(lane_base + col_acc + SNBP + g * 8 * W + kk * 8 + 4 * hh, l + kk * 4);
+                            }
+                            tmem_ld_wait();
+                            if (on && n0 < p.N) {
+#pragma unroll
+                                for (int j4 = 0; j4 < W; ++j4) {  // global columns n0 + 4hh*W + 4*j4 .. +3
+                                    float o[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int m = 4 * j4 + e, ch = m / W, kk = m % W;
+                                        o[e] = __uint_as_float(l[kk * 4 + ch]) - __uint_as_float(h[kk * 4 + ch]);
+                                    }
+                                    red_add_f4(dst_row + n0 + 4 * hh * W + 4 * j4, o[0], o[1], o[2], o[3]);
+                                }
+                            }
+                        }
+                    };
+                    if (p.rclass == 2) flush_rows(p.col_du1, p.dU + static_cast<size_t>(128 + row) * p.N, 128 + row < p.R);
+                    if (p.rclass == 0) {
+                        flush_rows(0u, row < 64 ? p.dU + static_cast<size_t>(row) * p.N : p.db,
+                                   row < p.R || row == 64);
+                    } else {
+                        flush_rows(0u, p.dU + static_cast<size_t>(row) * p.N, row < p.R);
+                        flush_rows(p.col_db, p.db, row == 0);
                     }
                 }
                 tc_fence_before();
@@ -413,9 +432,11 @@ static dsc_status launch_dudb(const LowrankArgs &a, const DeviceInfo &dev)
     p.R = a.R;
     p.N = a.D * a.W;
     p.n_mt = (p.BT + kM - 1) / kM;
-    const long long units = static_cast<long long>((a.D + SCB - 1) / SCB) * p.n_mt;
+    const int n_nb = (a.D + SCB - 1) / SCB;
+    const long long units = static_cast<long long>((n_nb + 1) / 2) * p.n_mt;  // (block pair, token tile) units
     if (units > 0x7fffffffLL) return DSC_ERR_UNSUPPORTED;
     p.n_units = static_cast<int>(units);
+    p.n_units_odd = (n_nb / 2) * p.n_mt;
     p.rclass = a.R <= 64 ? 0 : a.R <= 128 ? 1 : 2;
     p.kchunks = p.rclass == 0 ? 1 : p.rclass == 1 ? 2 : 4;  // z chunks of 64 columns (TMA zero-fills past R)
     p.col_du1 = NM;
@@ -448,8 +469,8 @@ static dsc_status launch_dudb(const LowrankArgs &a, const DeviceInfo &dev)
     auto kern = lowrank_bwd_dudb<W, SCB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return DSC_ERR_CUDA;
-    const int grid = dev.sm_count < p.n_units ? dev.sm_count : p.n_units;
-    return launch_overlapped(kern, grid, kThreads, smem, a.stream, tm_z, tm_x, tm_dy, p);
+    const int pairs = dev.sm_count / 2 < p.n_units ? dev.sm_count / 2 : p.n_units;
+    return launch_overlapped(kern, 2 * pairs, kThreads, smem, a.stream, tm_z, tm_x, tm_dy, p);
 }
 
 template <int W>

@@ -118,9 +118,11 @@ dsc_status dsc_lowrank_fwd(const void *x, const void *z, const void *U, const fl
 
 /*
  * Bytes of caller-provided device workspace dsc_lowrank_bwd needs for these
- * sizes: 16 * (D*W + 256) rounded up to 256, independent of B, T and R.  The
- * workspace holds the generator bias split into bf16 high and low halves,
- * one 16-byte row per group of 8 filter entries, written by the call itself.
+ * sizes: 16 * (D*W + 256) rounded up to 1024, plus 2 * R * D*W rounded up to
+ * 256; independent of B and T.  The call writes into it the generator bias
+ * split into bf16 high and low halves (one 16-byte row per filter entry) and a
+ * copy of U, both with the W taps of each group of 8 channels reordered
+ * tap-major.
  */
 size_t dsc_lowrank_bwd_workspace_bytes(int B, int T, int D, int W, int R);
 
@@ -150,12 +152,13 @@ dsc_status dsc_lowrank_bwd(const void *x, const void *z, const void *U, const fl
  * memory pool under a fixed memory plan, or a latency-critical loop that must
  * never enter the allocator.  The paper has no counterpart; this is an
  * interface convenience.  Same arguments and results as dsc_lowrank_bwd,
- * without `workspace`: the bias rows go to a fixed array of 2 MiB in the
+ * without `workspace`: the workspace lives in a fixed array of 8 MiB in the
  * library's static device memory, held by every GPU that loads the library
  * until the process exits.  Nothing is allocated or freed by the call, and no
  * allocating library routine is used.
- *   Limit: D*W + 256 <= 131,072 (the array holds that many 16-byte rows);
- *   larger sizes return DSC_ERR_INVALID_ARG before anything is launched.
+ *   Limit: dsc_lowrank_bwd_workspace_bytes(B, T, D, W, R) <= 8 MiB (about
+ *   2 * R * D*W + 16 * D*W bytes); larger sizes return DSC_ERR_INVALID_ARG
+ *   before anything is launched.
  *   The first call on a device looks up the array's device address (once per
  *   device and context, with that device current); make that first call
  *   before any stream capture.

@@ -114,13 +114,15 @@ def test_rejects_bad_arguments_before_any_launch(L):
     assert L.dsc_lowrank_fwd(p, p, p, p, p, 1, 8, 64, 4, 0, bf16, None, 0, None) == 1
     assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, 0, bf16, None, 0, None) == 1
     assert L.dsc_lowrank_bwd(p, p, p, p, None, p, p, p, p, None, 1, 8, 64, 4, 16, bf16, None, 0, None) == 1  # no dy
-    # the backward's workspace: 16 bytes per filter column (the bias rows) and 256 rows of padding, whatever
-    # B, T and R; a null workspace is refused
+    # the backward's workspace: 16 bytes per filter column (the bias rows) and 256 rows of padding, rounded up
+    # to 1 KB, then the reordered copy of U (2 bytes per element), whatever B and T; a null workspace is refused
     for b, t, r in ((8, 2048, 8), (1, 5, 64), (8, 2048, 256)):
-        assert L.dsc_lowrank_bwd_workspace_bytes(b, t, 2048, 4, r) == 16 * (2048 * 4 + 256)
+        rows = (16 * (2048 * 4 + 256) + 1023) // 1024 * 1024
+        assert L.dsc_lowrank_bwd_workspace_bytes(b, t, 2048, 4, r) == rows + (2 * r * 2048 * 4 + 255) // 256 * 256
     assert L.dsc_lowrank_bwd(p, p, p, p, p, p, p, p, p, None, 1, 8, 64, 4, 16, bf16, None, 0, None) == 1
-    # the allocation-free entry point holds at most D*W + 256 = 131072 rows in its array
-    assert L.dsc_lowrank_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 8, 32712, 4, 16, bf16, None, 0, None) == 1
+    # the allocation-free entry point's array holds 8 MiB of workspace: D = 16384, W = 4, R = 64 needs 9 MiB
+    assert L.dsc_lowrank_bwd_workspace_bytes(1, 8, 16384, 4, 64) > 8 << 20
+    assert L.dsc_lowrank_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 8, 16384, 4, 64, bf16, None, 0, None) == 1
     assert L.dsc_validate_cu_seqlens(None, 3, 1, 8, None) == 1
     # static convolution: the same size, W, dtype and alignment rules; dw must be fp32-aligned
     assert L.dsc_static_fwd(p, p, p, 0, 8, 64, 4, bf16, None, 0, None) == 1

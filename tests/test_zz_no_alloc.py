@@ -69,12 +69,39 @@ def test_noalloc_large_against_the_oracle(oracle_mod):
 def test_noalloc_rejects_sizes_beyond_its_array():
     import dynamic_short_convolution_gb300 as dsc
 
-    B, T, W, R = 1, 4, 4, 16
-    for D in (32712, 40000):  # D*W + 256 = 131104 (one 8-channel group over the 131072 rows) and more
-        x = torch.zeros(B, T, D, dtype=torch.bfloat16, device=DEV)
+    limit = 8 << 20  # bytes of the library's fixed workspace array
+    B, T, W, R = 1, 4, 4, 64
+    # the smallest channel count (a multiple of 8) whose workspace no longer fits, and one well past it
+    D = 8
+    while dsc.dsc_lowrank_bwd_workspace_bytes(B, T, D, W, R) <= limit:
+        D += 8
+    assert dsc.dsc_lowrank_bwd_workspace_bytes(B, T, D - 8, W, R) <= limit
+    for Dx in (D, 2 * D):
+        x = torch.zeros(B, T, Dx, dtype=torch.bfloat16, device=DEV)
         z = torch.zeros(B, T, R, dtype=torch.bfloat16, device=DEV)
-        U = torch.zeros(R, D * W, dtype=torch.bfloat16, device=DEV)
-        b = torch.zeros(D * W, dtype=torch.float32, device=DEV)
+        U = torch.zeros(R, Dx * W, dtype=torch.bfloat16, device=DEV)
+        b = torch.zeros(Dx * W, dtype=torch.float32, device=DEV)
         with pytest.raises(dsc.DscError) as e:
             dsc.dsc_lowrank_bwd_noalloc(x, z, U, b, x)
         assert e.value.status == dsc.DSC_ERR_INVALID_ARG
+
+
+def test_noalloc_at_its_limit_matches_regular_entry_point():
+    """The largest channel count whose workspace still fits the fixed array (the prep kernel's writes reach
+    the array's last bytes): results equal the regular entry point's."""
+    import dynamic_short_convolution_gb300 as dsc
+
+    limit = 8 << 20
+    B, T, W, R = 1, 40, 4, 64
+    D = 8
+    while dsc.dsc_lowrank_bwd_workspace_bytes(B, T, D + 8, W, R) <= limit:
+        D += 8
+    wl = inputs.custom(B, T, D, W, R=R, dtype="bf16", seed_id=884, packed=True, doc_min=2, doc_max=30)
+    g = _dev(inputs.make(wl))
+    args = (g["x"], g["z"], g["U"], g["bias"], g["dy"])
+    got = dsc.dsc_lowrank_bwd_noalloc(*args, cu_seqlens=g["cu_seqlens"])
+    assert dsc.dsc_sync_status() == dsc.DSC_OK
+    ref = dsc.dsc_lowrank_bwd(*args, cu_seqlens=g["cu_seqlens"])
+    assert dsc.dsc_sync_status() == dsc.DSC_OK
+    for name, a, b in zip(("dx", "dz", "dU", "db"), got, ref):
+        assert_close(a, b.double().cpu().numpy(), "bf16", f"noalloc at limit {name}")
