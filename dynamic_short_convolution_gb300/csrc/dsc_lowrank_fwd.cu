@@ -21,7 +21,7 @@
 // tap k): the W taps of one channel are adjacent accumulator columns, so tap
 // pairs feed packed fp32x2 math straight from TMEM registers.
 #include "dsc_internal.h"
-#include "dsc_tcgen05.cuh"
+#include "dsc_lowrank_common.cuh"  // swizzled tile offsets (swzt), swizzle_for; tcgen05 wrappers
 
 namespace dsc {
 
@@ -61,14 +61,6 @@ struct Header {
 
 }  // namespace lrf
 
-// Byte offset of 16-byte chunk `c` of row `row` in a swizzled tile whose rows are RB bytes (128 or 64).
-template <int RB>
-__device__ __forceinline__ uint32_t swz(int row, int c)
-{
-    if constexpr (RB == 128) return row * 128 + ((c ^ (row & 7)) << 4);
-    else return row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
-}
-
 template <int W, int CB>
 __global__ void __launch_bounds__(lrf::kThreads, 1)
     lowrank_fwd_tc(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_x,
@@ -79,8 +71,10 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     constexpr int NB = CB * W;         // filter columns per block (MMA N)
     constexpr int RB = CB * 2;         // bytes per x / y tile row
     constexpr int GROUPS = CB / 8;     // 8-channel groups per block
-    constexpr int GPW = GROUPS / 4;    // groups per epilogue warp (four warps per lane quadrant)
-    static_assert(NB % 16 == 0 && NB <= 256, "MMA N");
+    constexpr int NCW = GROUPS < 4 ? GROUPS : 4;  // epilogue warps with work per lane quadrant
+    constexpr int GPW = GROUPS / NCW;  // groups per working epilogue warp
+    constexpr int YB = RB / NCW;       // bytes of a warp's y staging row (its CB / NCW channels)
+    static_assert(NB % 16 == 0 && NB <= 256 && GROUPS % NCW == 0, "MMA N, channel groups");
     constexpr uint32_t IDESC = idesc_bf16_f32(kM, NB, false, true);        // A z K-major, B U MN-major
     constexpr uint32_t IDESC_BIAS = idesc_bf16_f32(kM, NB, false, false);  // A ones, B bias tile, both K-major
 
@@ -91,18 +85,18 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
     uint8_t *u_s = base + p.u_off;       // [NB/64 blocks][Rp rows][128 B]: U of the block, 128-B swizzled
     uint8_t *bt_s = base + p.bt_off;     // bias as an MMA B tile: [NB rows][16 K], no swizzle
     uint8_t *one_s = base + p.one_off;   // all-ones MMA A tile [128 rows][16 K]
-    uint8_t *y_s = base + p.y_off;       // per epilogue warp: 2 x [32 rows][RB/4] staging for its own stores
+    uint8_t *y_s = base + p.y_off;       // per working epilogue warp: 2 x [32 rows][YB] staging for its own stores
     uint8_t *stages = base + p.st_off;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nstages; ++s) {
             mbar_init(&hdr->full[s], 1);
-            mbar_init(&hdr->empty[s], 1 + kEpiWarps);
+            mbar_init(&hdr->empty[s], 1 + 4 * NCW);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&hdr->tmem_full[b], 1);
-            mbar_init(&hdr->tmem_empty[b], kEpiWarps);
+            mbar_init(&hdr->tmem_empty[b], 4 * NCW);
         }
         mbar_init(&hdr->u_full, 1);
         mbar_init(&hdr->u_free, 1);
@@ -259,14 +253,14 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             }
             __syncwarp();
         }
-    } else {
-        // ---------------- epilogue: y = x + sum_k acc_k * x~_k (the bias is inside acc).  Each warp
-        // owns 32 tokens x CB/4 channels of the tile and stores them itself (TMA, private double
+    } else if (((warp - kEpiWarp0) >> 2) < NCW) {
+        // ---------------- epilogue: y = x + sum_k acc_k * x~_k (the bias is inside acc).  Each working
+        // warp owns 32 tokens x CB/NCW channels of the tile and stores them itself (TMA, private double
         // buffer), so no warp ever waits for another one.
         const int q = warp & 3;                          // TMEM lane quadrant
-        const int h = (warp - kEpiWarp0) >> 2;           // which quarter of the channel groups
+        const int h = (warp - kEpiWarp0) >> 2;           // which share of the channel groups
         const int row = q * 32 + lane;                   // token within the tile
-        uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * (RB / 4));
+        uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * YB);
         DocCursor cursor;  // this thread's token increases from tile to tile within a block
         int i = 0;
         int s = 0;
@@ -295,7 +289,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             tc_fence_after();
             const uint8_t *st = stages + s * p.stage_bytes;
             const uint8_t *xs = st + p.x_off_in_stage;
-            uint8_t *ys = ywarp + b * (32 * (RB / 4));
+            uint8_t *ys = ywarp + b * (32 * YB);
             bool ys_free = false;  // this warp's store from two tiles ago has left buffer b
             const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;
 #pragma unroll
@@ -306,7 +300,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 uint32_t xw[W][4];           // x~ rows row-k of the group's 8 channels, bf16 pairs
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swz<RB>(row + (W - 1) - k, g));
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swzt<RB>(row + (W - 1) - k, g));
                     xw[k][0] = raw.x;
                     xw[k][1] = raw.y;
                     xw[k][2] = raw.z;
@@ -353,7 +347,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                     __syncwarp();
                     ys_free = true;
                 }
-                *reinterpret_cast<uint4 *>(ys + lane * (RB / 4) + gi * 16) = o;
+                *reinterpret_cast<uint4 *>(ys + lane * YB + gi * 16) = o;
             }
             // accumulator and x tile read: hand them back; store this warp's y sub-tile
             tc_fence_before();
@@ -363,7 +357,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
                 mbar_arrive(&hdr->tmem_empty[b]);
                 mbar_arrive(&hdr->empty[s]);
                 const int t0 = mt * kM;
-                tma_store_2d(&tm_y, ys, nb * CB + h * (CB / 4), t0 + q * 32);
+                tma_store_2d(&tm_y, ys, nb * CB + h * (CB / NCW), t0 + q * 32);
                 tma_store_commit();
             }
         }
@@ -390,6 +384,7 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
 {
     using namespace lrf;
     constexpr int NB = CB * W, RB = CB * 2, XR = kM + W - 1;
+    constexpr int NCW = CB / 8 < 4 ? CB / 8 : 4;
     Params p{};
     p.U = static_cast<const __nv_bfloat16 *>(a.U);
     p.bias = a.bias;
@@ -418,7 +413,7 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     p.one_off = align_up(off, 1024);
     off = p.one_off + kM * 32;
     p.y_off = align_up(off, 1024);
-    off = p.y_off + kEpiWarps * 2 * 32 * (RB / 4);
+    off = p.y_off + kEpiWarps * 2 * 32 * (RB / NCW);
     p.st_off = align_up(off, 1024);
     p.z_bytes = p.kchunks * 16384;
     p.x_off_in_stage = p.z_bytes;
@@ -426,7 +421,9 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     p.nv_off_in_stage = align_up(p.x_off_in_stage + p.x_bytes, 128);
     p.stage_bytes = align_up(p.nv_off_in_stage + kM, 1024);
     const unsigned fixed = 2048 + p.st_off;
-    if (static_cast<unsigned>(dev.max_smem_optin) < fixed + 2 * p.stage_bytes) return DSC_ERR_UNSUPPORTED;
+    // ranks above 128 leave room for one stage at their channel block (loads then wait for the tile before)
+    if (static_cast<unsigned>(dev.max_smem_optin) < fixed + (a.R > 128 ? 1 : 2) * p.stage_bytes)
+        return DSC_ERR_UNSUPPORTED;
     int ns = static_cast<int>((dev.max_smem_optin - fixed) / p.stage_bytes);
     p.nstages = ns > kMaxStages ? kMaxStages : ns;
     const unsigned smem = fixed + p.nstages * p.stage_bytes;
@@ -434,14 +431,14 @@ static dsc_status launch_lowrank_fwd(const LowrankArgs &a, const DeviceInfo &dev
     p.wait_ns = wait_limit_ns();
 
     CUtensorMap tm_z, tm_x, tm_y, tm_u;
-    const CUtensorMapSwizzle sw = RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle sw = swizzle_for(RB);  // 128, 64 or 32 bytes: the x tile's row width
     const unsigned long long BT = static_cast<unsigned long long>(p.BT);
     if (!encode_tmap_2d(&tm_z, a.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.R, BT, static_cast<unsigned long long>(a.R) * 2,
                         64, kM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.D, BT, static_cast<unsigned long long>(a.D) * 2,
                         CB, XR, sw) ||
         !encode_tmap_2d(&tm_y, a.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.D, BT, static_cast<unsigned long long>(a.D) * 2,
-                        CB / 4, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                        CB / NCW, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_tmap_2d(&tm_u, a.U, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.N, a.R, static_cast<unsigned long long>(p.N) * 2,
                         64, p.ksteps * 16, CU_TENSOR_MAP_SWIZZLE_128B))
         return DSC_ERR_CUDA;
@@ -456,7 +453,21 @@ dsc_status lowrank_fwd(const LowrankArgs &a)
 {
     DeviceInfo dev;
     if (!device_info(&dev)) return DSC_ERR_CUDA;
-    if (a.R > 128) return DSC_ERR_UNSUPPORTED;
+    if (a.R > 256) return DSC_ERR_UNSUPPORTED;
+    if (a.R > 128) {
+        // the block's U holds R rows: narrower channel blocks keep it resident beside a stage
+        switch (a.W) {
+        case 1: return launch_lowrank_fwd<1, 32>(a, dev);
+        case 2: return launch_lowrank_fwd<2, 32>(a, dev);
+        case 3: return launch_lowrank_fwd<3, 32>(a, dev);
+        case 4: return launch_lowrank_fwd<4, 32>(a, dev);
+        case 5: return launch_lowrank_fwd<5, 32>(a, dev);
+        case 6: return launch_lowrank_fwd<6, 32>(a, dev);
+        case 7: return launch_lowrank_fwd<7, 16>(a, dev);
+        case 8: return launch_lowrank_fwd<8, 16>(a, dev);
+        default: return DSC_ERR_INVALID_ARG;
+        }
+    }
     switch (a.W) {
     case 1: return launch_lowrank_fwd<1, 64>(a, dev);
     case 2: return launch_lowrank_fwd<2, 64>(a, dev);

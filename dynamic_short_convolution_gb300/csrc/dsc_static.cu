@@ -20,6 +20,8 @@
 // slot (p mod (W-1)) holding the input at document position p; the token's position also says how much
 // history its document has.  One thread per 16-byte chunk of channels: it reads the chunk's history,
 // writes y, then overwrites the slot of the oldest history token with this token's input.
+#include <type_traits>
+
 #include "dsc_dense_common.cuh"
 #include "dsc_tcgen05.cuh"  // named_bar
 
@@ -85,17 +87,20 @@ inline bool make_plan(const StaticArgs &a, bool bwd, int TT, int NCW, int W, int
     const int fit = static_cast<int>((static_cast<unsigned>(dev.max_smem_optin) - header) / p->stage_bytes);
     if (fit < 2) return false;
     p->nstages = fit < stage_cap ? fit : stage_cap;
-    // the backward's dw reduction reuses the stages: NCW partials of kDC * W fp32 values
-    if (bwd && static_cast<unsigned>(NCW * kDC * W * 4) > p->nstages * p->stage_bytes) return false;
+    // the backward's dw reduction reuses the stages: NCW partials of kDC * W values (fp32 for bf16 inputs,
+    // fp64 for fp32 inputs)
+    if (bwd && static_cast<unsigned>(NCW * kDC * W * 2 * es) > p->nstages * p->stage_bytes) return false;
     p->smem = header + p->nstages * p->stage_bytes;
     const long long BT = static_cast<long long>(a.B) * a.T;
     const long long n_tt = (BT + TT - 1) / TT;
     if (n_tt > 0x7fffffffLL) return false;
     p->n_tt = static_cast<int>(n_tt);
     p->n_cb = (a.D + kDC - 1) / kDC;
-    // CTAs per channel block: as many as fill the SMs, never more than the block has tiles
+    // CTAs per channel block: as many as fill the SMs, never more than the block has tiles.  The fp32
+    // backward gives each channel block to one CTA, which sums its dw in fp64 and stores it once (no fp32
+    // additions across CTAs), so that dw is the exactly rounded fp64 sum up to the partials' own rounding.
     int cpb = dev.sm_count / p->n_cb;
-    if (cpb < 1) cpb = 1;
+    if (cpb < 1 || (bwd && es == 4)) cpb = 1;
     if (cpb > p->n_tt) cpb = p->n_tt;
     p->cpb = cpb;
     p->grid = cpb * p->n_cb;
@@ -323,11 +328,14 @@ __global__ void __launch_bounds__(32 * (1 + stc::Tile<E, true>::NCW), 1)
     float2 wp[4][W];
     static_filter<E, W>(static_cast<const E *>(p.w), c, cvalid, wp);
     E *dx = static_cast<E *>(p.out0);
-    float2 dwp[4][W];  // dw partials of this lane's channel pairs, summed over every token this warp sees
+    // dw partials of this lane's 8 channels, summed over every token this warp sees: fp32 pairs for bf16
+    // inputs (exact products), fp64 for fp32 inputs
+    using Acc = typename std::conditional<std::is_same<E, float>::value, double, float>::type;
+    Acc dwp[8][W];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int k = 0; k < W; ++k) dwp[i][k] = make_float2(0.f, 0.f);
+        for (int k = 0; k < W; ++k) dwp[i][k] = Acc(0);
     int it = 0;
     for (int tt = j0; tt < p.n_tt; tt += p.cpb, ++it) {
         const int s = it % p.nstages;
@@ -379,8 +387,20 @@ __global__ void __launch_bounds__(32 * (1 + stc::Tile<E, true>::NCW), 1)
 #pragma unroll
                 for (int k = 0; k < W; ++k)
                     if (k < nv) {
+                        if constexpr (std::is_same<Acc, float>::value) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) dwp[i][k] = fma2(g[i], xw[ring(r - k, W)][i], dwp[i][k]);
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 v = fma2(g[i], xw[ring(r - k, W)][i], make_float2(dwp[2 * i][k], dwp[2 * i + 1][k]));
+                                dwp[2 * i][k] = v.x;
+                                dwp[2 * i + 1][k] = v.y;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                dwp[2 * i][k] = fma(static_cast<double>(g[i].x), static_cast<double>(xw[ring(r - k, W)][i].x), dwp[2 * i][k]);
+                                dwp[2 * i + 1][k] = fma(static_cast<double>(g[i].y), static_cast<double>(xw[ring(r - k, W)][i].y), dwp[2 * i + 1][k]);
+                            }
+                        }
                     }
             }
         }
@@ -391,24 +411,21 @@ __global__ void __launch_bounds__(32 * (1 + stc::Tile<E, true>::NCW), 1)
     // dw: the consumer warps' partials meet in shared memory (the stages are idle now: every tile this CTA
     // loaded has been consumed), then one fp32 addition per (channel, tap) of the block
     named_bar(1, NCW * 32);
-    float *red = reinterpret_cast<float *>(stages);  // [NCW][kDC][W]
-    float *mine = red + (warp - 1) * (kDC * W) + lane * 8 * W;
+    Acc *red = reinterpret_cast<Acc *>(stages);  // [NCW][kDC][W]
+    Acc *mine = red + (warp - 1) * (kDC * W) + lane * 8 * W;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int k = 0; k < W; ++k) {
-            mine[(2 * i) * W + k] = dwp[i][k].x;
-            mine[(2 * i + 1) * W + k] = dwp[i][k].y;
-        }
+        for (int k = 0; k < W; ++k) mine[i * W + k] = dwp[i][k];
     named_bar(1, NCW * 32);
     if (*abort_flag) return;
     for (int e = threadIdx.x - 32; e < kDC * W; e += NCW * 32) {
         const int ch = cb * kDC + e / W;
         if (ch >= p.D) continue;
-        float sum = 0.f;
+        Acc sum = Acc(0);
 #pragma unroll
         for (int q = 0; q < NCW; ++q) sum += red[q * (kDC * W) + e];
-        atomicAdd(p.dw + static_cast<size_t>(cb) * kDC * W + e, sum);
+        atomicAdd(p.dw + static_cast<size_t>(cb) * kDC * W + e, static_cast<float>(sum));
     }
 }
 
@@ -461,6 +478,24 @@ __global__ void static_bwd_dw_scalar(const E *__restrict__ x, const E *__restric
         const float g = Elem<E>::to_f(dy[i]);
         for (int k = 0; k < nv; ++k)
             atomicAdd(dw + d * W + k, g * Elem<E>::to_f(x[i - static_cast<long long>(k) * D]));
+    }
+}
+
+// fp32 inputs: one thread per (channel, tap) sums every token in fp64 and stores once
+__global__ void static_bwd_dw_scalar_f64(const float *__restrict__ x, const float *__restrict__ dy,
+                                         float *__restrict__ dw, int BT, int T, int D, int W, const int32_t *cu,
+                                         int n_docs)
+{
+    grid_dependency_wait();  // dw was zeroed two launches ago
+    const int n = D * W;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
+        const int d = e / W, k = e - d * W;
+        double acc = 0.0;
+        for (int t = 0; t < BT; ++t)
+            if (k < valid_taps(t, T, W, cu, n_docs))
+                acc = fma(static_cast<double>(dy[static_cast<size_t>(t) * D + d]),
+                          static_cast<double>(x[static_cast<size_t>(t - k) * D + d]), acc);
+        dw[e] = static_cast<float>(acc);
     }
 }
 
@@ -653,9 +688,14 @@ static dsc_status static_bwd_t(const StaticArgs &a, const DeviceInfo &dev)
                           a.T, a.D, a.W, a.cu, a.n_docs);
     if (s != DSC_OK) return s;
     // dx and dw are independent; the dw kernel follows the zeroing in stream order
-    return launch_overlapped(static_bwd_dw_scalar<E>, static_cast<unsigned>(blocks), 256u, 0, a.stream,
-                             static_cast<const E *>(a.x), static_cast<const E *>(a.dy), a.dw, a.B * a.T, a.T, a.D, a.W,
-                             a.cu, a.n_docs);
+    if constexpr (std::is_same<E, float>::value)
+        return launch_overlapped(static_bwd_dw_scalar_f64, static_cast<unsigned>((nw + 127) / 128), 128u, 0, a.stream,
+                                 a.x == nullptr ? nullptr : static_cast<const float *>(a.x),
+                                 static_cast<const float *>(a.dy), a.dw, a.B * a.T, a.T, a.D, a.W, a.cu, a.n_docs);
+    else
+        return launch_overlapped(static_bwd_dw_scalar<E>, static_cast<unsigned>(blocks), 256u, 0, a.stream,
+                                 static_cast<const E *>(a.x), static_cast<const E *>(a.dy), a.dw, a.B * a.T, a.T, a.D,
+                                 a.W, a.cu, a.n_docs);
 }
 
 dsc_status static_fwd(const StaticArgs &a)

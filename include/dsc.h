@@ -109,7 +109,7 @@ dsc_status dsc_bwd(const void *x, const void *w, const void *dy, void *dx, void 
  *   memory, then eq. 2 + eq. 3 with H = 1.
  *   x [B,T,D], z [B,T,R], U [R,D*W] in bf16, bias [D*W] fp32; writes y.
  *   Requirements: dt == DSC_BF16 (DSC_F32 -> DSC_ERR_UNSUPPORTED);
- *   D % 8 == 0; R % 8 == 0 and 8 <= R <= 128; 1 <= W <= 8; pointers 16-byte
+ *   D % 8 == 0; R % 8 == 0 and 8 <= R <= 256; 1 <= W <= 8; pointers 16-byte
  *   aligned.
  */
 dsc_status dsc_lowrank_fwd(const void *x, const void *z, const void *U, const float *bias, void *y, int B, int T,

@@ -40,6 +40,12 @@ SMALL = [
     (2, 140, 96, 6, 24, True),
     (1, 257, 136, 7, 112, True),
     (2, 33, 2048, 4, 64, True),
+    (1, 200, 256, 4, 192, True),     # R > 128: 32-channel blocks, one stage
+    (2, 150, 128, 4, 256, True),
+    (1, 140, 96, 1, 256, False),
+    (1, 130, 64, 6, 136, True),
+    (1, 150, 80, 7, 256, True),      # W = 7, R > 128: 16-channel blocks, two working warps per lane quadrant
+    (1, 129, 48, 8, 200, False),
 ]
 
 

@@ -25,16 +25,11 @@ def _dev(d):
 
 
 def _assert_dw(got, ref, mass, dtype, what="dw"):
-    """dw sums over every token.  bf16: the usual elementwise bound.  fp32: the usual bound plus 4e-6 of
-    the summands' l1 mass (sum_t |dy x~|), the scale of an fp32 sum's rounding error, which any
-    summation order may reach where the terms cancel."""
-    if dtype != "f32":
-        assert_close(got, ref, dtype, what)
-        return
+    """dw sums over every token; it is held to the same elementwise bound as every other output (fp32 inputs:
+    the library sums it in fp64 and rounds once).  `mass` (sum_t |dy x~|) is only reported."""
     g = to_np(got).reshape(ref.shape)
-    lim = 1e-5 * np.abs(ref) + 1e-6 + 4e-6 * mass
-    err = np.abs(g - ref)
-    assert (err <= lim).all(), f"{what}: max err {err.max():.3e}, worst ratio {(err / lim).max():.2f}"
+    assert np.isfinite(g).all() and mass.shape == ref.shape
+    assert_close(got, ref, dtype, what)
 
 
 # (B, T, D, W, packed, dtype): several token tiles, ragged tails, a ragged last channel block (D % 256),

@@ -63,7 +63,7 @@ def test_decode_guard_bands(dsc, shape):
     assert _intact(by, B * D) and _intact(bh, B * (W - 1) * D)
 
 
-@pytest.mark.parametrize("shape", [(2, 77, 192, 4, 32), (1, 260, 200, 3, 64), (2, 33, 136, 7, 16)])
+@pytest.mark.parametrize("shape", [(2, 77, 192, 4, 32), (1, 260, 200, 3, 64), (2, 33, 136, 7, 16), (1, 140, 72, 4, 256)])
 def test_lowrank_guard_bands(dsc, shape):
     B, T, D, W, R = shape
     d = inputs.make(inputs.custom(B, T, D, W, R=R, dtype="bf16", seed_id=962, packed=True, doc_min=1, doc_max=30))
@@ -105,12 +105,7 @@ def test_sweep_static(dsc, oracle_mod, case):
     assert_close(y.reshape(B * T, D), oracle_mod.static_fwd(d["x"], d["w"], W, cu_seqlens=cu), dt, "y")
     rdx, rdw = oracle_mod.static_bwd(d["x"], d["w"], d["dy"], W, cu_seqlens=cu)
     assert_close(dx.reshape(B * T, D), rdx, dt, "dx")
-    if dt == "bf16":
-        assert_close(dw, rdw, dt, "dw")
-    else:  # a sum over every token: fp32 bound plus 4e-6 of the summands' l1 mass
-        _, mass = oracle_mod.static_bwd(d["x"].abs(), d["w"], d["dy"].abs(), W, cu_seqlens=cu, want_dx=False)
-        err = (dw.double().cpu().numpy() - rdw).__abs__()
-        assert (err <= 1e-5 * abs(rdw) + 1e-6 + 4e-6 * mass).all()
+    assert_close(dw, rdw, dt, "dw")  # a sum over every token, held to the same bound as the other outputs
 
 
 @pytest.mark.parametrize("case", _sweep_cases(2027, 14), ids=str)
@@ -133,7 +128,7 @@ def test_sweep_dense(dsc, oracle_mod, case):
 @pytest.mark.parametrize("case", [c for c in _sweep_cases(2028, 16) if c[2] % 8 == 0][:10], ids=str)
 def test_sweep_lowrank(dsc, oracle_mod, case):
     B, T, D, W, packed, _ = case
-    R = random.Random(T + D).choice([16, 32, 48, 64])
+    R = random.Random(T + D).choice([16, 32, 48, 64, 96, 128, 192, 256])
     d = inputs.make(inputs.custom(B, T, D, W, R=R, dtype="bf16", seed_id=990 + T % 11, packed=packed, doc_min=1,
                                   doc_max=25))
     g = {k: (v.to(DEV) if v is not None else None) for k, v in d.items()}
