@@ -20,6 +20,11 @@ for real activations):
 * ``static_bf16``   B=8 T=2048 D=2048 W=4 bf16, one filter w [D, W] for every token
   (eq. 1), w = 0.1*N(0,1) + 0.5 on tap k=0: the head-wise workload's shape and
   filter statistics, so the static and dynamic kernels can be compared
+* ``proj_qkv_bf16`` B=4 T=8192 W=4 H=16 bf16 over packed documents like
+  ``qkv_packed_bf16``, but from the projection's input: h [B, T, Dm=2048] ~N(0,1),
+  the Q/K/V weights Wx [D=3072, Dm] ~N(0, 1/Dm) (so x = h Wx^T ~N(0,1)), the
+  filter generator Wg [(D/H)*W, Dm] ~N(0, 0.1/Dm) and its bias bg ~N(0,0.01) fp32
+  (so w = h Wg^T + bg has variance about 0.1, as in ``qkv_packed_bf16``)
 * ``decode_bf16``   B=512 sequences, one new token each, D=6144 (Q, K and V of a
   2048-wide model side by side), W=4 H=16 bf16; history ring [B, W-1, D] ~N(0,1),
   positions ~U{0..4095} (a fifth of them below W-1, where the document's history
@@ -28,7 +33,8 @@ for real activations):
 Upstream gradients dy ~ N(0,1) everywhere.  N(0, s) means variance s.
 Values are drawn in fp32 and rounded to nearest-even bf16 where the workload
 is bf16.  Seeds: 1000 * workload id + tensor index (x=0, w=1, dy=2, z=3, U=4,
-bias=5, document lengths=6, decode history=7, decode positions=8).
+bias=5, document lengths=6, decode history=7, decode positions=8, projection input h=0,
+Q/K/V weights=9, generator weights=10, generator bias=5).
 """
 from __future__ import annotations
 
@@ -37,14 +43,14 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-X, WGT, DY, Z, U, BIAS, LENS, HIST, POS = range(9)
+X, WGT, DY, Z, U, BIAS, LENS, HIST, POS, PWX, PWG = range(11)
 
 
 @dataclass(frozen=True)
 class Workload:
     wid: int
     name: str
-    kind: str            # "dense" (materialised / head-wise), "lowrank", "static" or "decode"
+    kind: str            # "dense" (materialised / head-wise), "lowrank", "static", "decode" or "proj"
     B: int
     T: int
     D: int
@@ -76,6 +82,8 @@ WORKLOADS = {
     5: Workload(5, "qkv_packed_bf16", "dense", 4, 8192, 3072, 4, H=16, w_std=math.sqrt(0.1), packed=True),
     6: Workload(6, "static_bf16", "static", 8, 2048, 2048, 4, w_std=0.1, w_tap0=0.5),
     7: Workload(7, "decode_bf16", "decode", 512, 1, 6144, 4, H=16, w_std=0.1, w_tap0=0.5, extra={"max_pos": 4096}),
+    8: Workload(8, "proj_qkv_bf16", "proj", 4, 8192, 3072, 4, H=16, w_std=math.sqrt(0.1), packed=True,
+                extra={"Dm": 2048}),
 }
 
 
@@ -129,6 +137,8 @@ def make(wl: Workload, with_grad: bool = True) -> dict:
     dt = wl.torch_dtype
     if wl.kind == "decode":
         return make_decode(wl)
+    if wl.kind == "proj":
+        return make_proj(wl)
     out = {"x": _normal((wl.B, wl.T, wl.D), 1.0, wl.wid, X, dt)}
     if wl.kind == "static":
         w = torch.randn(wl.D, wl.W, generator=_gen(wl.wid, WGT), dtype=torch.float32)
@@ -194,6 +204,25 @@ def make_on_device(wl: Workload, device, with_grad: bool = True) -> dict:
     cu = doc_offsets(wl)
     out["cu_seqlens"] = None if cu is None else cu.to(device)
     return out
+
+
+def make_proj(wl: Workload) -> dict:
+    """The projection's input h [B, T, Dm], the Q/K/V weights Wx [D, Dm], the generator's weights
+    Wg [(D/H)*W, Dm] (row g*W + k) and bias bg [(D/H)*W] fp32, and the document offsets."""
+    dt = wl.torch_dtype
+    Dm = int(wl.extra["Dm"])
+    NG = (wl.D // wl.H) * wl.W
+    return {"h": _normal((wl.B, wl.T, Dm), 1.0, wl.wid, X, dt),
+            "Wx": _normal((wl.D, Dm), 1.0 / math.sqrt(Dm), wl.wid, PWX, dt),
+            "Wg": _normal((NG, Dm), wl.w_std / math.sqrt(Dm), wl.wid, PWG, dt),
+            "bg": _normal((NG,), 0.1, wl.wid, BIAS, torch.float32),
+            "cu_seqlens": doc_offsets(wl)}
+
+
+def custom_proj(B, T, Dm, D, W, H=1, seed_id=500, w_std=0.5, packed=False, doc_min=1, doc_max=None) -> Workload:
+    """A projection workload of arbitrary shape for tests (seeded by ``seed_id``)."""
+    return Workload(seed_id, "custom_proj", "proj", B, T, D, W, H=H, w_std=w_std, packed=packed, doc_min=doc_min,
+                    doc_max=doc_max if doc_max is not None else T, extra={"Dm": Dm})
 
 
 def make_decode(wl: Workload) -> dict:

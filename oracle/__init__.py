@@ -18,6 +18,8 @@ section "Key design 1"):
 * ``static_fwd``:  y = x + sum_k w[d, k] * x~[t-k, d]                  (eq. 1 with the residual of eq. 3)
 * ``static_bwd``:  dx rows and dw [D, W] (summed over every token) of <dy, y>
 * ``decode_step``: y of one new token per sequence against a history ring (eq. 2 + eq. 3, one step)
+* ``proj_fwd``:    y of eq. 2 + 3 with x = h Wx^T and w = h Wg^T + bg computed from the projection's input
+                   h ("Placement": the generator's projection beside the Q/K/V projection)
 
 Every function takes tensors laid out exactly like the CUDA library's
 arguments: x, y, dy, dx ``[B, T, D]``; head-wise / materialised w
@@ -31,7 +33,9 @@ low-rank parameter gradients to a list of filter columns.
 Parity status: every function here is pinned, by ``tests/test_oracle.py`` and
 ``tests/test_oracle_static_decode.py`` (library conv1d, closed forms,
 invariants, finite differences, adjoint identities, a decode chain equal to
-the full forward, and a hand-computed golden fixture).
+the full forward, and a hand-computed golden fixture); ``proj_fwd`` by
+``tests/test_oracle_proj.py`` (numpy's matmul followed by the pinned ``fwd``,
+closed forms for a zero generator and one-hot generator biases, causality).
 """
 from __future__ import annotations
 
@@ -79,6 +83,7 @@ def _load():
             lib.dsco_static_fwd_rows.argtypes = [vp, vp, i32, i64, i64, i32, vp, i64, i64, vp]
             lib.dsco_static_bwd.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i64, i64, vp, vp]
             lib.dsco_decode_step.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i64, vp]
+            lib.dsco_proj_fwd_rows.argtypes = [vp, vp, vp, vp, i32, i32, i64, i64, i64, i32, i64, vp, i64, i64, vp]
             _lib = lib
     return _lib
 
@@ -283,4 +288,28 @@ def decode_step(x, w, hist, pos, W: int, H: int) -> np.ndarray:
     y = np.empty((B, D), dtype=np.float64)
     _load().dsco_decode_step(px, pw, ph, _ptr(pz), dt, B, D, W, H, _ptr(y))
     del kx, kw, kh
+    return y
+
+
+def proj_fwd(h, Wx, Wg, bg, W: int, H: int, cu_seqlens=None, rows=None) -> np.ndarray:
+    """Projected form: h [B, T, Dm], Wx [D, Dm], Wg [(D/H)*W, Dm] (row g*W + k), bg [(D/H)*W] fp32 or None.
+    y rows [r0, r1) of eq. 2 + 3 on x = h Wx^T and w = h Wg^T + bg, float64 [r1-r0, D]."""
+    B, T, Dm = h.shape
+    D = Wx.shape[0]
+    BT = B * T
+    assert D % H == 0 and tuple(Wx.shape) == (D, Dm) and tuple(Wg.shape) == ((D // H) * W, Dm)
+    ph, ch, kh = _raw(h)
+    px, cx, kx = _raw(Wx)
+    pg, cg, kg = _raw(Wg)
+    dt = _same_dtype(ch, cx, cg)
+    if bg is None:
+        pb, cb, kb = None, _F32, None
+    else:
+        assert tuple(bg.shape) == ((D // H) * W,)
+        pb, cb, kb = _bias_ptr(bg)
+    ds = docstarts(B, T, cu_seqlens)
+    r0, r1 = _rows(rows, BT)
+    y = np.empty((r1 - r0, D), dtype=np.float64)
+    _load().dsco_proj_fwd_rows(ph, px, pg, pb, cb, dt, BT, Dm, D, W, H, _ptr(ds), r0, r1, _ptr(y))
+    del kh, kx, kg, kb
     return y

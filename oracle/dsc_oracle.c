@@ -35,6 +35,12 @@
  *   same residual and masking, its backward (dw summed over every token), and
  *   one decode step of eq. 2 + 3 against a per-sequence history ring.
  *
+ *   Projected form ("Placement": the filter generator's projection sits beside
+ *   the Q/K/V projection, and the convolution consumes both outputs):
+ *     x[t,d]   = sum_j h[t,j] Wx[d,j]
+ *     w[t,g,k] = sum_j h[t,j] Wg[g*W + k, j] + bg[g*W + k]
+ *   then eq. 2 + residual of eq. 3 on that x and w.
+ *
  * Tokens are indexed on the flattened B*T axis; docstart(t) >= (t / T) * T
  * always, so sequences never see each other.  Every product and sum is done
  * in IEEE double from inputs converted exactly (fp32, bf16 or fp64 storage).
@@ -329,5 +335,52 @@ void dsco_decode_step(const void *x, const void *w, const void *hist, const int3
             }
             y[b * D + d] = acc;
         }
+    }
+}
+
+/*
+ * Projected forward rows [r0, r1): for every output token t, the W input rows
+ * x[t-k] (those inside t's document) and the filter row w[t] are computed in
+ * fp64 from h, Wx, Wg and bg (bg may be NULL: no generator bias), then eq. 2 +
+ * residual.  h [BT, Dm], Wx [D, Dm], Wg [(D/H)*W, Dm] share one storage type;
+ * bg has its own (bdt).
+ */
+void dsco_proj_fwd_rows(const void *h, const void *Wx, const void *Wg, const void *bg, int bdt, int dt, int64_t BT,
+                        int64_t Dm, int64_t D, int W, int64_t H, const int64_t *ds, int64_t r0, int64_t r1,
+                        double *y)
+{
+    const int64_t G = D / H, NG = G * W;
+    (void)BT;
+#pragma omp parallel
+    {
+        double *xr = (double *)malloc(sizeof(double) * (size_t)(W * D)); /* xr[k*D + d] = x[t-k, d] */
+        double *wr = (double *)malloc(sizeof(double) * (size_t)NG);       /* wr[g*W + k] = w[t, g, k] */
+#pragma omp for schedule(static)
+        for (int64_t t = r0; t < r1; ++t) {
+            for (int k = 0; k < W; ++k) {
+                const int64_t j = t - k;
+                for (int64_t d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    if (j >= ds[t])
+                        for (int64_t i = 0; i < Dm; ++i)
+                            acc += load(h, dt, j * Dm + i) * load(Wx, dt, d * Dm + i);
+                    xr[k * D + d] = acc;
+                }
+            }
+            for (int64_t n = 0; n < NG; ++n) {
+                double acc = bg ? load(bg, bdt, n) : 0.0;
+                for (int64_t i = 0; i < Dm; ++i)
+                    acc += load(h, dt, t * Dm + i) * load(Wg, dt, n * Dm + i);
+                wr[n] = acc;
+            }
+            for (int64_t d = 0; d < D; ++d) {
+                double acc = xr[d];
+                for (int k = 0; k < W; ++k)
+                    acc += wr[(d / H) * W + k] * xr[k * D + d];
+                y[(t - r0) * D + d] = acc;
+            }
+        }
+        free(xr);
+        free(wr);
     }
 }
