@@ -5,8 +5,9 @@
 (notes on "Dynamic Short Convolutions Improve Transformers", eq. 2 with the
 residual of eq. 3), forward and backward, with materialised, head-wise and
 low-rank fused filters, over packed documents; the static short convolution
-(eq. 1) on the same machinery; and a single-token decode step against a
-per-sequence history ring.  The compute lives in
+(eq. 1) on the same machinery; a single-token decode step against a
+per-sequence history ring; and the projection that produces the convolution's
+input and filter with the convolution applied in its epilogue.  The compute lives in
 ``libdsc.so`` (hand-written CUDA kernels behind a C ABI, ``include/dsc.h``);
 this package is a thin ctypes binding with the same function names, plus the
 build step and the seeded input generators used by tests and benchmarks.
@@ -31,6 +32,7 @@ from ._abi import (  # noqa: F401
     dsc_lowrank_bwd_noalloc,
     dsc_lowrank_bwd_workspace_bytes,
     dsc_lowrank_fwd,
+    dsc_proj_fwd,
     dsc_static_bwd,
     dsc_static_fwd,
     dsc_sync_status,

@@ -39,6 +39,7 @@ SIGNATURES = {
     "dsc_static_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "dsc_static_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "dsc_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "dsc_proj_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "dsc_validate_cu_seqlens": (_i, [_vp, _i, _i, _i, _vp]),
     "dsc_sync_status": (_i, [_vp]),
     "dsc_test_wait_timeout": (_i, [_u64, _vp]),
@@ -295,6 +296,27 @@ def dsc_decode_step(x, w, hist, pos, y=None, *, stream=None):
                               _dev(pos, "pos", torch.int32, device=dev), _dev(y, "y", x.dtype, x.shape, dev), B, D, W,
                               D // w.shape[1], _dt(x), _stream(stream))
     _check(s, "dsc_decode_step")
+    return y
+
+
+def dsc_proj_fwd(h, Wx, Wg, bg=None, y=None, *, W, cu_seqlens=None, stream=None):
+    """y of the convolution applied to the projection's outputs: x = h Wx^T, w = h Wg^T + bg, with
+    h [B,T,Dm], Wx [D,Dm], Wg [(D/H)*W, Dm] (row g*W + k), bg [(D/H)*W] fp32 or None; H = D*W / Wg rows."""
+    dev = _lead(h, "h", 3)
+    B, T, Dm = h.shape
+    if Wx.dim() != 2 or Wx.shape[1] != Dm or Wg.dim() != 2 or Wg.shape[1] != Dm or W < 1:
+        raise ValueError("shapes: h [B,T,Dm]; Wx [D,Dm]; Wg [(D/H)*W, Dm]")
+    D = Wx.shape[0]
+    if Wg.shape[0] % W or Wg.shape[0] == 0 or D % (Wg.shape[0] // W):
+        raise ValueError("Wg must have (D/H)*W rows for a head size H dividing D")
+    H = D // (Wg.shape[0] // W)
+    if y is None:
+        y = torch.empty(B, T, D, dtype=h.dtype, device=h.device)
+    bp = None if bg is None else _dev(bg, "bg", torch.float32, (Wg.shape[0],), dev)
+    cu, n = _cu(cu_seqlens, dev)
+    s = lib().dsc_proj_fwd(_dev(h, "h"), _dev(Wx, "Wx", h.dtype, device=dev), _dev(Wg, "Wg", h.dtype, device=dev), bp,
+                           _dev(y, "y", h.dtype, (B, T, D), dev), B, T, Dm, D, W, H, _dt(h), cu, n, _stream(stream))
+    _check(s, "dsc_proj_fwd")
     return y
 
 

@@ -318,6 +318,26 @@ dsc_status dsc_static_bwd(const void *x, const void *w, const void *dy, void *dx
     return static_bwd(a);
 }
 
+dsc_status dsc_proj_fwd(const void *h, const void *Wx, const void *Wg, const float *bg, void *y, int B, int T, int Dm,
+                        int D, int W, int H, dsc_dtype dt, const int32_t *cu_seqlens, int n_docs,
+                        cudaStream_t stream)
+{
+    if (dt != DSC_F32 && dt != DSC_BF16) return DSC_ERR_INVALID_ARG;
+    if (!dims_ok(B, T, D, W) || Dm < 1 || H < 1 || D % H != 0 || !cu_ok(cu_seqlens, n_docs))
+        return DSC_ERR_INVALID_ARG;
+    if (!h || !Wx || !Wg || !y) return DSC_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * T * Dm >= (1LL << 31)) return DSC_ERR_INVALID_ARG;
+    if (bg != nullptr && !elem_aligned(bg, 4)) return DSC_ERR_INVALID_ARG;
+    if (dt == DSC_F32) return DSC_ERR_UNSUPPORTED;
+    if (D % 8 != 0 || Dm % 8 != 0 || !(H == 1 || H == 2 || H == 4 || H % 8 == 0)) return DSC_ERR_UNSUPPORTED;
+    if (!aligned16(h) || !aligned16(Wx) || !aligned16(Wg) || !aligned16(y)) return DSC_ERR_UNSUPPORTED;
+    ProjArgs a;
+    a.h = h; a.Wx = Wx; a.Wg = Wg; a.bg = bg; a.y = y;
+    a.B = B; a.T = T; a.Dm = Dm; a.D = D; a.W = W; a.H = H;
+    a.cu = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0; a.stream = stream;
+    return proj_fwd(a);
+}
+
 dsc_status dsc_decode_step(const void *x, const void *w, void *hist, const int32_t *pos, void *y, int B, int D, int W,
                            int H, dsc_dtype dt, cudaStream_t stream)
 {

@@ -70,6 +70,20 @@ struct DecodeArgs {
     cudaStream_t stream = nullptr;
 };
 
+// Arguments of the projection with the convolution in its epilogue (h [B,T,Dm]; Wx [D,Dm]; Wg [(D/H)W, Dm];
+// bg [(D/H)W] fp32 or nullptr; y [B,T,D]).
+struct ProjArgs {
+    const void *h = nullptr;
+    const void *Wx = nullptr;
+    const void *Wg = nullptr;
+    const float *bg = nullptr;
+    void *y = nullptr;
+    int B = 0, T = 0, Dm = 0, D = 0, W = 0, H = 0;
+    const int32_t *cu = nullptr;
+    int n_docs = 0;
+    cudaStream_t stream = nullptr;
+};
+
 dsc_status dense_fwd(const DenseArgs &a);
 dsc_status dense_bwd(const DenseArgs &a);
 dsc_status lowrank_fwd(const LowrankArgs &a);
@@ -83,6 +97,7 @@ dsc_status lowrank_bwd_dudb(const LowrankArgs &a, const DeviceInfo &dev);  // se
 dsc_status static_fwd(const StaticArgs &a);
 dsc_status static_bwd(const StaticArgs &a);
 dsc_status decode_step(const DecodeArgs &a);
+dsc_status proj_fwd(const ProjArgs &a);
 
 // Device address of a file-scope __device__ variable on the current device, looked up once per device
 // and context (looked up again after the context changes, e.g. after cudaDeviceReset).

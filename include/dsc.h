@@ -220,6 +220,33 @@ dsc_status dsc_decode_step(const void *x, const void *w, void *hist, const int32
                            int H, dsc_dtype dt, cudaStream_t stream);
 
 /*
+ * dsc_proj_fwd -- the projection that produces the convolution's input and its
+ *   filter, with eq. 2 + eq. 3 applied in the projection GEMM's epilogue
+ *   ("Placement": the filter generator's projection beside the Q/K/V
+ *   projection; fusing the convolution into the matmul epilogue saves the
+ *   round trip of x and w through memory):
+ *     x[t,d]   = sum_j h[t,j] Wx[d,j]                     (never stored)
+ *     w[t,g,k] = sum_j h[t,j] Wg[g*W + k, j] + bg[g*W+k]  (never stored)
+ *     y[t,d]   = x[t,d] + sum_{k<W} w[t, d/H, k] * x~[t-k, d]
+ *   with the zero history and document masking of dsc_fwd.
+ *     h  [B,T,Dm]         the projection's input, bf16
+ *     Wx [D,Dm]           one row per output channel (the layout of a linear
+ *                         layer's weight), bf16
+ *     Wg [(D/H)*W, Dm]    the generator: row g*W + k is tap k of head g, bf16
+ *     bg [(D/H)*W]        the generator's bias, fp32; may be NULL (no bias)
+ *     y  [B,T,D]          bf16, overwritten
+ *   x and w are accumulated in fp32 on the tensor cores and used unrounded.
+ *   Requirements: dt == DSC_BF16 (DSC_F32 -> DSC_ERR_UNSUPPORTED); D, Dm
+ *   multiples of 8; D % H == 0 with H in {1, 2, 4} or a multiple of 8, and a
+ *   tile of whole heads must fit 256 accumulator columns (H <= 128 for
+ *   W <= 8; else DSC_ERR_UNSUPPORTED); 1 <= W <= 8; h, Wx, Wg, y 16-byte
+ *   aligned, bg 4-byte aligned; B*T*max(D, Dm) < 2^31.
+ */
+dsc_status dsc_proj_fwd(const void *h, const void *Wx, const void *Wg, const float *bg, void *y, int B, int T, int Dm,
+                        int D, int W, int H, dsc_dtype dt, const int32_t *cu_seqlens, int n_docs,
+                        cudaStream_t stream);
+
+/*
  * dsc_validate_cu_seqlens -- device-side check of packed-document offsets:
  * cu[0] == 0, strictly increasing, cu[n_docs] == B*T.  Asynchronous; a
  * violation is recorded as DSC_ERR_INVALID_ARG in the device status word,
