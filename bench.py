@@ -369,8 +369,70 @@ class DecodeProblem:
         pass
 
 
+class ProjProblem:
+    """The projection with the convolution in its epilogue (forward only): h [B,T,Dm] and the weights in,
+    y out.  Algorithmic bytes: h read once, the weights once, y written once; flops: 2 B T Dm (D + (D/H) W).
+    ``unfused`` runs the same computation as a caller without the fused kernel would: cuBLAS GEMMs that
+    store x and w (bf16; the generator bias added in the GEMM), then dsc_fwd."""
+
+    def __init__(self, wl, dev):
+        import torch
+
+        from dynamic_short_convolution_gb300 import inputs
+
+        self.wl = wl
+        d = inputs.make(wl)
+        self.host = d
+        g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+        Dm = g["h"].shape[-1]
+        NG = g["Wg"].shape[0]
+        BT = wl.B * wl.T
+        t = {"h": g["h"], "Wx": g["Wx"], "Wg": g["Wg"], "bg": g["bg"], "cu": g["cu_seqlens"],
+             "y": torch.empty(wl.B, wl.T, wl.D, dtype=torch.bfloat16, device=dev),
+             "x": torch.empty(wl.B, wl.T, wl.D, dtype=torch.bfloat16, device=dev),
+             "w": torch.empty(wl.B, wl.T, wl.D // wl.H, wl.W, dtype=torch.bfloat16, device=dev)}
+        self.bg16 = g["bg"].to(torch.bfloat16)
+        hb = g["h"].numel() * 2
+        self.bytes_fwd = hb + (g["Wx"].numel() + g["Wg"].numel()) * 2 + 4 * NG + BT * wl.D * 2
+        self.bytes_bwd = 0
+        self.flops_fwd = 2 * BT * Dm * (wl.D + NG)
+        self.flops_bwd = 0
+        self.Dm = Dm
+        self.rot = _Sets({"h": t["h"]}, hb)  # only h is large; the weights stay in L2 as they would in a model
+        self.t = t
+        self.cur = t
+
+    def advance(self):
+        self.cur = dict(self.t, h=self.rot.next()["h"])
+
+    def fwd(self):
+        import dynamic_short_convolution_gb300 as dsc
+
+        c = self.cur
+        dsc.dsc_proj_fwd(c["h"], c["Wx"], c["Wg"], c["bg"], c["y"], W=self.wl.W, cu_seqlens=c["cu"])
+
+    def unfused(self, ev=None):
+        import torch
+
+        import dynamic_short_convolution_gb300 as dsc
+
+        c = self.cur
+        h2 = c["h"].view(-1, self.Dm)
+        torch.matmul(h2, c["Wx"].t(), out=c["x"].view(-1, self.wl.D))
+        if ev:
+            ev[0].record()
+        torch.addmm(self.bg16, h2, c["Wg"].t(), out=c["w"].view(h2.shape[0], -1))
+        if ev:
+            ev[1].record()
+        dsc.dsc_fwd(c["x"], c["w"], c["y"], cu_seqlens=c["cu"])
+
+    def bwd(self):
+        pass
+
+
 def make_problem(wl, dev):
-    return {"lowrank": LowrankProblem, "static": StaticProblem, "decode": DecodeProblem}.get(wl.kind, DenseProblem)(wl, dev)
+    return {"lowrank": LowrankProblem, "static": StaticProblem, "decode": DecodeProblem,
+            "proj": ProjProblem}.get(wl.kind, DenseProblem)(wl, dev)
 
 
 def time_graph_replay(prob, steps):
@@ -488,6 +550,8 @@ def _oracle_step(oracle, wl, d, r0, r1):
         c1 = max(c0 + 1, (r1 * nw) // BT)
         oracle.lowrank_bwd(d["x"], d["z"], d["U"], d["bias"], d["dy"], wl.W, cu_seqlens=d["cu_seqlens"],
                            cols=list(range(c0, min(c1, nw))), want=("dU", "db"))
+    elif wl.kind == "proj":  # the fused projection + convolution: forward rows [r0, r1) (no backward)
+        oracle.proj_fwd(d["h"], d["Wx"], d["Wg"], d["bg"], wl.W, wl.H, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
     elif wl.kind == "decode":  # one decode step of sequences [r0, r1) (no backward: inference)
         oracle.decode_step(d["x"][r0:r1], d["w"][r0:r1], d["hist"][r0:r1], d["pos"][r0:r1], wl.W, wl.H)
     else:
@@ -516,7 +580,7 @@ def cpu_rows(budget_s=2.5):
     for wl in inputs.WORKLOADS.values():
         v, n, spent = oracle_tokens_per_s(wl, budget_s=budget_s)
         r = {"cpu_tokens_per_s": v, "cpu_cores": cores,
-             "cpu_sample": f"{n} tokens of {wl.name} in {spent:.1f} s" + ("" if wl.kind == "decode" else ", fwd + bwd")}
+             "cpu_sample": f"{n} tokens of {wl.name} in {spent:.1f} s" + ("" if wl.kind in ("decode", "proj") else ", fwd + bwd")}
         if wl.wid == 1 and _omp_threads(1):
             v1, n1, s1 = oracle_tokens_per_s(wl, budget_s=budget_s)
             _omp_threads(cores)
@@ -804,6 +868,48 @@ def measure_e2e(prob, steps, dev, world):
                    "steps pipelined on three streams"}
 
 
+def measure_proj_row(prob, hbm_peak, tc_peak, reps=30):
+    """The fused projection + convolution against the unfused path, per call (CUDA events, medians)."""
+    import torch
+
+    wl = prob.wl
+    for _ in range(3):
+        prob.advance()
+        prob.fwd()
+        prob.unfused()
+    torch.cuda.synchronize()
+    fused, unf, gx, gw = [], [], [], []
+    for _ in range(reps):
+        prob.advance()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record()
+        prob.fwd()
+        e[1].record()
+        u = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        prob.advance()
+        u[0].record()
+        prob.unfused(ev=u[1:3])
+        u[3].record()
+        torch.cuda.synchronize()
+        fused.append(e[0].elapsed_time(e[1]))
+        unf.append(u[0].elapsed_time(u[3]))
+        gx.append(u[0].elapsed_time(u[1]))
+        gw.append(u[1].elapsed_time(u[2]))
+    mf, mu = statistics.median(fused), statistics.median(unf)
+    tf = prob.flops_fwd / (mf / 1e3) / 1e12
+    return {"fwd_us": 1e3 * mf, "tokens_per_s": wl.B * wl.T / (mf / 1e3), "fwd_tflops": tf,
+            "tensor_frac": tf / tc_peak, "fwd_bytes": prob.bytes_fwd, "fwd_flops": prob.flops_fwd,
+            "bound_us": 1e6 * max(prob.flops_fwd / (tc_peak * 1e12), prob.bytes_fwd / (hbm_peak * 1e9)),
+            "roofline_frac": 1e6 * prob.flops_fwd / (tc_peak * 1e12) / (1e3 * mf),
+            "unfused_us": 1e3 * mu, "unfused_gemm_x_us": 1e3 * statistics.median(gx),
+            "unfused_gemm_w_us": 1e3 * statistics.median(gw),
+            "unfused_conv_us": 1e3 * (mu - statistics.median(gx) - statistics.median(gw)),
+            "speedup_vs_unfused": mu / mf,
+            "unfused_path": "torch.matmul (cuBLAS) for x, torch.addmm for w with its bias, both stored bf16, then "
+                            "dsc_fwd",
+            "timing": f"median of {reps} calls, CUDA events, h rotated over copies larger than L2"}
+
+
 def measure_rows(dev, hbm_peak, tc_peak, only=None):
     """Every workload (or the one named `only`), timed the same way (fewer steps): fwd / bwd device time and
     roofline fractions."""
@@ -823,6 +929,11 @@ def measure_rows(dev, hbm_peak, tc_peak, only=None):
                 prob.fwd()
                 prob.bwd()
             torch.cuda.synchronize()
+            if wl.kind == "proj":
+                out[wl.name] = measure_proj_row(prob, hbm_peak, tc_peak)
+                del prob
+                torch.cuda.empty_cache()
+                continue
             if wl.kind == "decode":
                 ms = time_back_to_back(prob, 200)
                 gms = time_graph_replay(prob, 200)

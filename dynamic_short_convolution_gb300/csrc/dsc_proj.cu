@@ -8,6 +8,9 @@
 //   acc[t, c]       = sum_j h[t, j] Wx[n0 + c, j]          c < CBX        x of the tile's channels
 //   acc[t, CBX + i] = sum_j h[t, j] Wg[g0 W + i, j]        i < GB         their heads' filters (+ bg)
 //   y[t, c] = x[t, c] + sum_{k<W} w[t, c/H, k] x~[t-k, c]                 eq. 2 + eq. 3
+// x[t] (the residual and tap 0) is used as accumulated, in fp32; the earlier
+// tokens' x[t-k] of taps k >= 1 is rounded to bf16 first, as it would be had
+// the projection stored it (which halves the warp exchange that delivers it).
 //
 // Only y is written: x and w live in the TMEM accumulator and never reach HBM.
 //
@@ -18,15 +21,15 @@
 // tokens.  K (the projection's input width Dm) runs in steps of 64 through a
 // TMA ring (128-byte swizzle, K-major A and B; B = Wx rows then Wg rows).
 // Warps: a TMA producer, the MMA issuer (which owns TMEM), and 8 epilogue
-// warps, two per TMEM lane quadrant, each taking half of the tile's channels.
+// warps, two per TMEM lane quadrant, each taking every other 8-channel group.
 // Two accumulators in TMEM (2 x 256 columns): the MMAs of the next tile run
 // while the epilogue works on this one.  The epilogue reads the tap-k input
-// x[t-k] from lane - k by warp shuffles; the first W-1 lanes of a quadrant
-// take it from the previous quadrant's last rows, exchanged through shared
-// memory once per tile (one named barrier, which also carries the warps'
-// common abort decision).
+// x[t-k] from lane - k by a warp rotation; for it, the last W-1 lanes of a
+// quadrant offer the previous quadrant's last rows (exchanged through shared
+// memory once per tile, behind one named barrier that also carries the warps'
+// common abort decision), which is what the first lanes need.
 #include "dsc_internal.h"
-#include "dsc_tcgen05.cuh"
+#include "dsc_lowrank_common.cuh"  // warp_wait (bounded, suspending), tcgen05 wrappers
 
 namespace dsc {
 
@@ -102,7 +105,7 @@ __global__ void __launch_bounds__(prj::kThreads, 1)
     uint8_t *base = smem_raw + 1024;
     base += (1024u - (smem_u32(base) & 1023u)) & 1023u;
     uint8_t *stages = base + p.st_off;            // [A: 128 rows x 128 B][B: NP rows x 128 B] per stage
-    float *bnd = reinterpret_cast<float *>(base + p.bnd_off);  // [2][4 quadrants][2 halves][groups][W-1][8]
+    uint32_t *bnd = reinterpret_cast<uint32_t *>(base + p.bnd_off);  // [2][4 quadrants][CBX/8 groups][W-1][4 bf16 pairs]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(prj::kThreads, 1)
             const int r0 = mt * MO - (W - 1);           // first token row of the tile (may be negative: zeros)
             const int n0 = nt * p.CBX, g0 = (n0 / p.H) * W;
             for (int ks = 0; ks < p.ksteps; ++ks, ++k) {
-                if (k >= p.nstages) ok = mbar_wait(&hdr->empty[s], ph ^ 1, p.wait_ns);
+                if (k >= p.nstages) ok = warp_wait(&hdr->empty[s], ph ^ 1, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
                 if (!ok) break;
                 if (lane == 0) {
@@ -185,13 +188,13 @@ __global__ void __launch_bounds__(prj::kThreads, 1)
         bool ok = true;
         for (int li = 0; li < n_local && ok; ++li) {
             const int b = li & 1;
-            if (li >= 2) ok = mbar_wait(&hdr->tempty[b], ((li >> 1) & 1) ^ 1, p.wait_ns);
+            if (li >= 2) ok = warp_wait(&hdr->tempty[b], ((li >> 1) & 1) ^ 1, p.wait_ns);
             ok = __all_sync(0xffffffffu, ok) && (*abort_flag == 0);
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + b * kAccCols;
             for (int ks = 0; ks < p.ksteps; ++ks, ++k) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&hdr->full[s], ph, p.wait_ns)) && (*abort_flag == 0);
+                ok = warp_wait(&hdr->full[s], ph, p.wait_ns) && (*abort_flag == 0);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
@@ -216,13 +219,16 @@ __global__ void __launch_bounds__(prj::kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue: warp (lane quadrant q, channel half hf): rows 32q .. 32q+31 of the tile
+        // ---------------- epilogue: warp (lane quadrant q, column warp cw): rows 32q .. 32q+31 of the tile,
+        // every (kEpiWarps / 4)-th 8-channel group of its G = CBX / 8, from group cw
         const int ew = warp - kEpiWarp0;
-        const int q = warp & 3, hf = ew >> 2;
+        const int q = warp & 3, cw = ew >> 2;
         const int row = q * 32 + lane;
         const bool halo_row = row < W - 1;                // the tokens before the tile: inputs only
+        const bool tail = lane >= 32 - (W - 1);           // this lane's row is among the quadrant's last W-1
+        const int tj = lane - (32 - (W - 1));             // its index among them (tail lanes)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        const int gph = p.CBX / 16;                       // 8-channel groups per half
+        const int G = p.CBX / 8;
         DocCursor cursor;
         bool ok = true;
         for (int li = 0; li < n_local; ++li) {
@@ -233,24 +239,21 @@ __global__ void __launch_bounds__(prj::kThreads, 1)
             const int t = mt * MO - (W - 1) + row;        // this thread's token
             const int nv = (t >= 0 && t < p.BT) ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;
             const bool full_taps = __all_sync(0xffffffffu, nv == W);
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(&hdr->tfull[b], (li >> 1) & 1, p.wait_ns));
+            ok = ok && warp_wait(&hdr->tfull[b], (li >> 1) & 1, p.wait_ns);
             tc_fence_after();
             const uint32_t acc = lane_base + b * kAccCols;
-            float *bq = bnd + (b * 8 + q * 2 + hf) * (gph * HB * 8);  // this warp's slots
-            // pass 1: the last W-1 rows of this quadrant, for the quadrant below
+            // pass 1: the last W-1 rows of this quadrant (x of every group of this warp), for the quadrant below
             if (ok && W > 1) {
-                for (int gi = 0; gi < gph; ++gi) {
+                for (int g = cw; g < G; g += kEpiWarps / 4) {
                     uint32_t xv[8];
-                    tmem_ld_x8(acc + hf * (p.CBX / 2) + gi * 8, xv);
+                    tmem_ld_x8(acc + g * 8, xv);
                     tmem_ld_wait();
-                    const int j = lane - (32 - (W - 1));
-                    if (j >= 0) {
-                        float4 *dst = reinterpret_cast<float4 *>(bq + (gi * HB + j) * 8);
-                        dst[0] = make_float4(__uint_as_float(xv[0]), __uint_as_float(xv[1]), __uint_as_float(xv[2]),
-                                             __uint_as_float(xv[3]));
-                        dst[1] = make_float4(__uint_as_float(xv[4]), __uint_as_float(xv[5]), __uint_as_float(xv[6]),
-                                             __uint_as_float(xv[7]));
-                    }
+                    if (tail)
+                        *reinterpret_cast<uint4 *>(bnd + (((b * 4 + q) * G + g) * HB + tj) * 4) = make_uint4(
+                            pack_bf16x2(__uint_as_float(xv[0]), __uint_as_float(xv[1])),
+                            pack_bf16x2(__uint_as_float(xv[2]), __uint_as_float(xv[3])),
+                            pack_bf16x2(__uint_as_float(xv[4]), __uint_as_float(xv[5])),
+                            pack_bf16x2(__uint_as_float(xv[6]), __uint_as_float(xv[7])));
                 }
             }
             // every epilogue warp reaches this barrier once per tile, and they decide together whether to stop
@@ -258,51 +261,58 @@ __global__ void __launch_bounds__(prj::kThreads, 1)
                 ok = false;
                 break;
             }
-            const float *bprev = bnd + (b * 8 + ((q + 3) & 3) * 2 + hf) * (gph * HB * 8);  // quadrant q-1
-            // pass 2: eq. 2 + 3 for every 8-channel group of this half
-            for (int gi = 0; gi < gph; ++gi) {
-                const int lc0 = hf * (p.CBX / 2) + gi * 8;  // first channel of the group within the tile
+            // pass 2: eq. 2 + 3 for this warp's groups
+            for (int g = cw; g < G; g += kEpiWarps / 4) {
+                const int lc0 = g * 8;                    // first channel of the group within the tile
                 const int c0 = n0 + lc0;
                 uint32_t xv[8], wv[WC];
                 tmem_ld_x8(acc + lc0, xv);
                 tmem_ld_n<WC>(acc + p.CBX + (lc0 / p.H) * W, wv);
-                float bgv[WC];
-                const int gcol = (c0 / p.H) * W;  // generator row of the group's first head, first tap
+                // tail lanes: the previous quadrant's row of the same tail index (rows before the tile for
+                // quadrant 0, whose lanes below W-1 are not stored)
+                uint4 e4 = make_uint4(0u, 0u, 0u, 0u);  // bf16 pairs of channels (0,1) .. (6,7)
+                if (tail && q > 0 && W > 1) e4 = *reinterpret_cast<const uint4 *>(bnd + (((b * 4 + q - 1) * G + g) * HB + tj) * 4);
+                float wk[WC];
+                const int gcol = (c0 / p.H) * W;          // generator row of the group's first head, first tap
+                const bool in_range = c0 < p.D;
 #pragma unroll
-                for (int i = 0; i < WC; ++i) bgv[i] = (p.bg != nullptr && c0 < p.D) ? __ldg(p.bg + gcol + i) : 0.f;
+                for (int i = 0; i < WC; ++i) wk[i] = (p.bg != nullptr && in_range) ? __ldg(p.bg + gcol + i) : 0.f;
                 tmem_ld_wait();
-                float xf[8], yv[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    xf[c] = __uint_as_float(xv[c]);
-                    yv[c] = xf[c];
+                for (int i = 0; i < WC; ++i) wk[i] += __uint_as_float(wv[i]);
+                float xf[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) xf[c] = __uint_as_float(xv[c]);
+                // tap k of channel c: wk[hx(c) * W + k], hx(c) the channel's head within the group
+                auto wpair = [&](int c, int kk) {
+                    const int h0 = HG > 1 ? c / (8 / HG) : 0, h1 = HG > 1 ? (c + 1) / (8 / HG) : 0;
+                    return make_float2(wk[h0 * W + kk], wk[h1 * W + kk]);
+                };
+                float2 y2[4];
+                uint32_t xp[4];  // this row's x as bf16 pairs: what the earlier taps of the rows below read
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const float2 x2 = make_float2(xf[2 * e2], xf[2 * e2 + 1]);
+                    y2[e2] = fma2(wpair(2 * e2, 0), x2, x2);  // residual + tap 0, unrounded
+                    xp[e2] = pack_bf16x2(x2.x, x2.y);
                 }
+                const uint32_t ep[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
-                for (int kk = 0; kk < W; ++kk) {
-                    float xk[8];
-                    if (kk == 0) {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) xk[c] = xf[c];
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) xk[c] = __shfl_up_sync(0xffffffffu, xf[c], kk);
-                        if (lane < kk) {  // row 32q + lane - kk lies in quadrant q-1 (quadrant 0: halo rows only)
-                            const float *src = bprev + (gi * HB + (W - 1) - (kk - lane)) * 8;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) xk[c] = q > 0 ? src[c] : 0.f;
-                        }
-                    }
+                for (int kk = 1; kk < W; ++kk) {
+                    // x[t-k] (bf16, as a stored projection output would be): a rotation by kk lanes; lanes >= 32-kk
+                    // offer the previous quadrant's tail rows
                     const bool on = full_taps || kk < nv;  // x~ is zero before the token's document start
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int hx = HG > 1 ? c / (8 / HG) : 0;  // the channel's head within the group
-                        const float wk = __uint_as_float(wv[hx * W + kk]) + bgv[hx * W + kk];
-                        yv[c] = on ? fmaf(wk, xk[c], yv[c]) : yv[c];
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        uint32_t v = __shfl_sync(0xffffffffu, lane >= 32 - kk ? ep[e2] : xp[e2], (lane - kk) & 31);
+                        v = on ? v : 0u;
+                        y2[e2] = fma2(wpair(2 * e2, kk),
+                                      make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u)), y2[e2]);
                     }
                 }
-                if (!halo_row && t < p.BT && c0 < p.D) {
-                    const uint4 o = make_uint4(pack_bf16x2(yv[0], yv[1]), pack_bf16x2(yv[2], yv[3]),
-                                               pack_bf16x2(yv[4], yv[5]), pack_bf16x2(yv[6], yv[7]));
+                if (!halo_row && t < p.BT && in_range) {
+                    const uint4 o = make_uint4(pack_bf16x2(y2[0].x, y2[0].y), pack_bf16x2(y2[1].x, y2[1].y),
+                                               pack_bf16x2(y2[2].x, y2[2].y), pack_bf16x2(y2[3].x, y2[3].y));
                     *reinterpret_cast<uint4 *>(p.y + static_cast<size_t>(t) * p.D + c0) = o;
                 }
             }
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(prj::kThreads, 1)
     }
 
     // ---- teardown: nothing of this CTA may still be in flight
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0) {  // every copy issued has landed (at once, unless the CTA gave up early)
         for (int s = 0; s < p.nstages; ++s)
             if (issued_last[s] >= 0) (void)mbar_wait(&hdr->full[s], (issued_last[s] / p.nstages) & 1, kDrainLimitNs);
     }
@@ -380,8 +390,8 @@ static dsc_status launch_proj(const ProjArgs &a, const DeviceInfo &dev)
     p.ksteps = (a.Dm + kK - 1) / kK;
     p.a_bytes = kM * 128;
     p.stage_bytes = align_up(p.a_bytes + p.NP * 128, 1024);
-    const int gph = p.CBX / 16, hb = W > 1 ? W - 1 : 1;
-    p.bnd_half = static_cast<unsigned>(8 * gph * hb * 8 * 4);
+    const int hb = W > 1 ? W - 1 : 1;
+    p.bnd_half = static_cast<unsigned>(4 * (p.CBX / 8) * hb * 16);  // one buffer: 4 quadrants x groups x rows, 16 B
     p.bnd_off = 0;
     p.st_off = align_up(2 * p.bnd_half, 1024);
     const unsigned room = static_cast<unsigned>(dev.max_smem_optin) - 2048 - p.st_off;
