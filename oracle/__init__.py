@@ -20,6 +20,8 @@ section "Key design 1"):
 * ``decode_step``: y of one new token per sequence against a history ring (eq. 2 + eq. 3, one step)
 * ``proj_fwd``:    y of eq. 2 + 3 with x = h Wx^T and w = h Wg^T + bg computed from the projection's input
                    h ("Placement": the generator's projection beside the Q/K/V projection)
+* ``lowrank_zproj_fwd``: the low-rank form with its code z = h W1^T computed from the layer input h
+                   ("Parameterization": the generator maps D -> R -> W*D)
 
 Every function takes tensors laid out exactly like the CUDA library's
 arguments: x, y, dy, dx ``[B, T, D]``; head-wise / materialised w
@@ -84,6 +86,8 @@ def _load():
             lib.dsco_static_bwd.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i64, i64, vp, vp]
             lib.dsco_decode_step.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i64, vp]
             lib.dsco_proj_fwd_rows.argtypes = [vp, vp, vp, vp, i32, i32, i64, i64, i64, i32, i64, vp, i64, i64, vp]
+            lib.dsco_lowrank_zproj_fwd_rows.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i64, i64, i32, i64, vp,
+                                                         i64, i64, vp]
             _lib = lib
     return _lib
 
@@ -190,6 +194,29 @@ def lowrank_fwd(x, z, U, bias, W: int, cu_seqlens=None, rows=None) -> np.ndarray
     y = np.empty((r1 - r0, D), dtype=np.float64)
     _load().dsco_lowrank_fwd_rows(px, pz, pu, pb, cb, dt, BT, D, W, R, _ptr(ds), r0, r1, _ptr(y))
     del kx, kz, ku, kb
+    return y
+
+
+def lowrank_zproj_fwd(x, h, W1, U, bias, W: int, cu_seqlens=None, rows=None) -> np.ndarray:
+    """Low-rank form with the generator's first projection: z = h W1^T (h [B, T, Dm], W1 [R, Dm]), then the
+    filter z U + bias and eq. 2 + 3 on x.  y rows [r0, r1), float64 [r1-r0, D]."""
+    B, T, D = x.shape
+    Dm = h.shape[-1]
+    R = W1.shape[0]
+    BT = B * T
+    assert tuple(h.shape) == (B, T, Dm) and tuple(W1.shape) == (R, Dm)
+    assert tuple(U.shape) == (R, D * W) and tuple(bias.shape) == (D * W,)
+    px, cx, kx = _raw(x)
+    ph, ch, kh = _raw(h)
+    p1, c1, k1 = _raw(W1)
+    pu, cu_, ku = _raw(U)
+    pb, cb, kb = _bias_ptr(bias)
+    dt = _same_dtype(cx, ch, c1, cu_)
+    ds = docstarts(B, T, cu_seqlens)
+    r0, r1 = _rows(rows, BT)
+    y = np.empty((r1 - r0, D), dtype=np.float64)
+    _load().dsco_lowrank_zproj_fwd_rows(px, ph, p1, pu, pb, cb, dt, BT, Dm, D, W, R, _ptr(ds), r0, r1, _ptr(y))
+    del kx, kh, k1, ku, kb
     return y
 
 

@@ -180,6 +180,50 @@ void dsco_lowrank_fwd_rows(const void *x, const void *z, const void *U, const vo
     }
 }
 
+/*
+ * Low-rank forward with the generator's first projection ("Parameterization":
+ * the generator maps the layer input through D -> R -> W*D; "Placement": its
+ * first projection runs beside the Q/K/V projection): rows [r0, r1) of
+ *   z[t, r]  = sum_i h[t, i] W1[r, i]                    (the rank-R code)
+ *   Wt[t, n] = sum_r z[t, r] U[r, n] + bias[n]            n = d*W + k
+ *   y[t, d]  = x[t, d] + sum_k Wt[t, d*W+k] * x~[t-k, d]
+ * all in fp64.  h [BT, Dm], W1 [R, Dm], x [BT, D], U [R, D*W] share one
+ * storage type; bias has its own (bdt).
+ */
+void dsco_lowrank_zproj_fwd_rows(const void *x, const void *h, const void *W1, const void *U, const void *bias, int bdt,
+                                 int dt, int64_t BT, int64_t Dm, int64_t D, int W, int64_t R, const int64_t *ds,
+                                 int64_t r0, int64_t r1, double *y)
+{
+    const int64_t NW = D * W;
+    (void)BT;
+#pragma omp parallel
+    {
+        double *zr = (double *)malloc(sizeof(double) * (size_t)R);
+        double *wrow = (double *)malloc(sizeof(double) * (size_t)NW);
+#pragma omp for schedule(static)
+        for (int64_t t = r0; t < r1; ++t) {
+            for (int64_t r = 0; r < R; ++r) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < Dm; ++i) acc += load(h, dt, t * Dm + i) * load(W1, dt, r * Dm + i);
+                zr[r] = acc;
+            }
+            for (int64_t n = 0; n < NW; ++n) {
+                double acc = load(bias, bdt, n);
+                for (int64_t r = 0; r < R; ++r) acc += zr[r] * load(U, dt, r * NW + n);
+                wrow[n] = acc;
+            }
+            for (int64_t d = 0; d < D; ++d) {
+                double acc = load(x, dt, t * D + d);
+                for (int k = 0; k < W; ++k)
+                    acc += wrow[d * W + k] * xt(x, dt, D, ds, t, t - k, d);
+                y[(t - r0) * D + d] = acc;
+            }
+        }
+        free(zr);
+        free(wrow);
+    }
+}
+
 /* G[t, d*W+k] = dy[t,d] * xt(t, t-k, d): the gradient of the loss w.r.t. the generated filter. */
 static double gfil(const void *x, const void *dy, int dt, int64_t D, int W, const int64_t *ds, int64_t t, int64_t n)
 {
