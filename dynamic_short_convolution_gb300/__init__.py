@@ -4,7 +4,8 @@
 
 (notes on "Dynamic Short Convolutions Improve Transformers", eq. 2 with the
 residual of eq. 3), forward and backward, with materialised, head-wise and
-low-rank fused filters, over packed documents; the static short convolution
+low-rank fused filters (the low-rank generator's first projection on chip
+too), over packed documents; the static short convolution
 (eq. 1) on the same machinery; a single-token decode step against a
 per-sequence history ring; and the projection that produces the convolution's
 input and filter with the convolution applied in its epilogue.  The compute lives in
@@ -32,6 +33,7 @@ from ._abi import (  # noqa: F401
     dsc_lowrank_bwd_noalloc,
     dsc_lowrank_bwd_workspace_bytes,
     dsc_lowrank_fwd,
+    dsc_lowrank_zproj_fwd,
     dsc_proj_fwd,
     dsc_static_bwd,
     dsc_static_fwd,

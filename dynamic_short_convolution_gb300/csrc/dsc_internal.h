@@ -86,7 +86,22 @@ struct ProjArgs {
 
 dsc_status dense_fwd(const DenseArgs &a);
 dsc_status dense_bwd(const DenseArgs &a);
+// Low-rank forward whose code z = h W1^T is computed on chip from the layer input h.
+struct LowrankZArgs {
+    const void *x = nullptr;
+    const void *h = nullptr;
+    const void *W1 = nullptr;
+    const void *U = nullptr;
+    const float *bias = nullptr;
+    void *y = nullptr;
+    int B = 0, T = 0, D = 0, Dm = 0, W = 0, R = 0;
+    const int32_t *cu = nullptr;
+    int n_docs = 0;
+    cudaStream_t stream = nullptr;
+};
+
 dsc_status lowrank_fwd(const LowrankArgs &a);
+dsc_status lowrank_zproj_fwd(const LowrankZArgs &a);
 dsc_status lowrank_bwd(const LowrankArgs &a);
 size_t lowrank_bwd_workspace(int B, int T, int D, int W, int R);
 dsc_status lowrank_bwd_validate(const void *x, const void *z, const void *U, const float *bias, const void *dy, void *dx,
