@@ -430,9 +430,62 @@ class ProjProblem:
         pass
 
 
+class ZprojProblem:
+    """The low-rank forward with the generator's first projection on chip (forward only): x, the layer input
+    h and the weights in, y out.  Algorithmic bytes: x, h, W1, U and the bias read once, y written once;
+    flops: the two projections, 2 B T R (Dm + D W).  ``unfused`` is the caller's path without the fused kernel:
+    z = h W1^T by cuBLAS, stored bf16, then dsc_lowrank_fwd."""
+
+    def __init__(self, wl, dev):
+        import torch
+
+        from dynamic_short_convolution_gb300 import inputs
+
+        self.wl = wl
+        d = inputs.make(wl)
+        g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+        BT = wl.B * wl.T
+        Dm = g["h"].shape[-1]
+        self.Dm = Dm
+        t = {"x": g["x"], "h": g["h"], "W1": g["W1"], "U": g["U"], "bias": g["bias"], "cu": g["cu_seqlens"],
+             "y": torch.empty(wl.B, wl.T, wl.D, dtype=torch.bfloat16, device=dev),
+             "z": torch.empty(wl.B, wl.T, wl.R, dtype=torch.bfloat16, device=dev)}
+        per = (g["x"].numel() + g["h"].numel()) * 2
+        self.bytes_fwd = per + (g["W1"].numel() + g["U"].numel()) * 2 + 4 * g["bias"].numel() + BT * wl.D * 2
+        self.bytes_bwd = 0
+        self.flops_fwd = 2 * BT * wl.R * (Dm + wl.D * wl.W)
+        self.flops_bwd = 0
+        self.rot = _Sets({"x": t["x"], "h": t["h"]}, per)
+        self.t = t
+        self.cur = t
+
+    def advance(self):
+        self.cur = dict(self.t, **self.rot.next())
+
+    def fwd(self):
+        import dynamic_short_convolution_gb300 as dsc
+
+        c = self.cur
+        dsc.dsc_lowrank_zproj_fwd(c["x"], c["h"], c["W1"], c["U"], c["bias"], c["y"], cu_seqlens=c["cu"])
+
+    def unfused(self, ev=None):
+        import torch
+
+        import dynamic_short_convolution_gb300 as dsc
+
+        c = self.cur
+        torch.matmul(c["h"].view(-1, self.Dm), c["W1"].t(), out=c["z"].view(-1, self.wl.R))
+        if ev:
+            ev[0].record()
+        dsc.dsc_lowrank_fwd(c["x"], c["z"], c["U"], c["bias"], c["y"], cu_seqlens=c["cu"])
+
+    def bwd(self):
+        pass
+
+
 def make_problem(wl, dev):
     return {"lowrank": LowrankProblem, "static": StaticProblem, "decode": DecodeProblem,
-            "proj": ProjProblem}.get(wl.kind, DenseProblem)(wl, dev)
+            "proj": ProjProblem, "zproj": ZprojProblem}.get(wl.kind, DenseProblem)(wl, dev)
 
 
 def time_graph_replay(prob, steps):
@@ -552,6 +605,9 @@ def _oracle_step(oracle, wl, d, r0, r1):
                            cols=list(range(c0, min(c1, nw))), want=("dU", "db"))
     elif wl.kind == "proj":  # the fused projection + convolution: forward rows [r0, r1) (no backward)
         oracle.proj_fwd(d["h"], d["Wx"], d["Wg"], d["bg"], wl.W, wl.H, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
+    elif wl.kind == "zproj":  # the low-rank forward with z from the layer input: rows [r0, r1) (no backward)
+        oracle.lowrank_zproj_fwd(d["x"], d["h"], d["W1"], d["U"], d["bias"], wl.W, cu_seqlens=d["cu_seqlens"],
+                                 rows=(r0, r1))
     elif wl.kind == "decode":  # one decode step of sequences [r0, r1) (no backward: inference)
         oracle.decode_step(d["x"][r0:r1], d["w"][r0:r1], d["hist"][r0:r1], d["pos"][r0:r1], wl.W, wl.H)
     else:
@@ -580,7 +636,7 @@ def cpu_rows(budget_s=2.5):
     for wl in inputs.WORKLOADS.values():
         v, n, spent = oracle_tokens_per_s(wl, budget_s=budget_s)
         r = {"cpu_tokens_per_s": v, "cpu_cores": cores,
-             "cpu_sample": f"{n} tokens of {wl.name} in {spent:.1f} s" + ("" if wl.kind in ("decode", "proj") else ", fwd + bwd")}
+             "cpu_sample": f"{n} tokens of {wl.name} in {spent:.1f} s" + ("" if wl.kind in ("decode", "proj", "zproj") else ", fwd + bwd")}
         if wl.wid == 1 and _omp_threads(1):
             v1, n1, s1 = oracle_tokens_per_s(wl, budget_s=budget_s)
             _omp_threads(cores)
@@ -910,6 +966,44 @@ def measure_proj_row(prob, hbm_peak, tc_peak, reps=30):
             "timing": f"median of {reps} calls, CUDA events, h rotated over copies larger than L2"}
 
 
+def measure_zproj_row(prob, hbm_peak, tc_peak, reps=30):
+    """The fused-code low-rank forward against the unfused path, per call (CUDA events, medians)."""
+    import torch
+
+    wl = prob.wl
+    for _ in range(3):
+        prob.advance()
+        prob.fwd()
+        prob.unfused()
+    torch.cuda.synchronize()
+    fused, unf, gz = [], [], []
+    for _ in range(reps):
+        prob.advance()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record()
+        prob.fwd()
+        e[1].record()
+        u = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        prob.advance()
+        u[0].record()
+        prob.unfused(ev=u[1:2])
+        u[2].record()
+        torch.cuda.synchronize()
+        fused.append(e[0].elapsed_time(e[1]))
+        unf.append(u[0].elapsed_time(u[2]))
+        gz.append(u[0].elapsed_time(u[1]))
+    mf, mu = statistics.median(fused), statistics.median(unf)
+    bound = max(prob.flops_fwd / (tc_peak * 1e12), prob.bytes_fwd / (hbm_peak * 1e9))
+    return {"fwd_us": 1e3 * mf, "tokens_per_s": wl.B * wl.T / (mf / 1e3), "fwd_bytes": prob.bytes_fwd,
+            "fwd_flops": prob.flops_fwd, "fwd_gbs": prob.bytes_fwd / mf / 1e6,
+            "fwd_hbm_frac": prob.bytes_fwd / mf / 1e6 / hbm_peak, "bound_us": 1e6 * bound,
+            "roofline_frac": 1e6 * bound / (1e3 * mf), "unfused_us": 1e3 * mu,
+            "unfused_gemm_z_us": 1e3 * statistics.median(gz),
+            "unfused_conv_us": 1e3 * (mu - statistics.median(gz)), "speedup_vs_unfused": mu / mf,
+            "unfused_path": "torch.matmul (cuBLAS) for z = h W1^T stored bf16, then dsc_lowrank_fwd",
+            "timing": f"median of {reps} calls, CUDA events, x and h rotated over copies larger than L2"}
+
+
 def measure_rows(dev, hbm_peak, tc_peak, only=None):
     """Every workload (or the one named `only`), timed the same way (fewer steps): fwd / bwd device time and
     roofline fractions."""
@@ -929,8 +1023,8 @@ def measure_rows(dev, hbm_peak, tc_peak, only=None):
                 prob.fwd()
                 prob.bwd()
             torch.cuda.synchronize()
-            if wl.kind == "proj":
-                out[wl.name] = measure_proj_row(prob, hbm_peak, tc_peak)
+            if wl.kind in ("proj", "zproj"):
+                out[wl.name] = (measure_proj_row if wl.kind == "proj" else measure_zproj_row)(prob, hbm_peak, tc_peak)
                 del prob
                 torch.cuda.empty_cache()
                 continue

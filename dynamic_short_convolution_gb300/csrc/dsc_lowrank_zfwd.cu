@@ -11,12 +11,14 @@
 // The code z is never stored: it lives in TMEM, then in shared memory as an
 // exact pair of bf16 halves (z_hi = bf16(z), z_lo = bf16(z - z_hi), together
 // z to about 16 significant bits) that is the A operand of the second
-// projection for every channel block of its token tile: [z_hi | z_lo | 1 1 0..]
-// against [U ; U ; b_hi ; b_lo ; 0..].
+// projection for every channel block of its token tile: [z_hi | z_lo] against
+// [U ; U], then an all-ones tile against the bias rows [b_hi ; b_lo ; 0..].
 //
-// Work unit: 128 tokens x one block of CB channels, ordered token-major.  Each
-// CTA owns whole token tiles (all their channel blocks), so the layer input h
-// of a tile is read once and its z computed once.  One ring of shared-memory slots carries two
+// Work unit: 128 tokens x one block of CB channels, ordered token-major; a
+// CTA takes a contiguous run of units, which covers one or two token tiles,
+// and computes z once for each tile it touches.  (Whole tiles per CTA read h
+// once but leave SMs idle when there are fewer tiles than SMs: measured
+// slower.)  One ring of shared-memory slots carries two
 // kinds of items in the order the CTA needs them: "z items" (two 64-wide K
 // chunks of the h tile and of W1) when a token tile starts, and one "unit
 // item" per unit (the block's U rows with the bias as two extra rows, and the
@@ -25,7 +27,7 @@
 //               each unit item (bf16 hi and lo, 14 zero rows after them)
 //   warp 1      TMEM owner; lane 0 issues the z MMAs (M=128, N=R, K=16) into
 //               the accumulator the tile's first unit will use, then per unit
-//               the filter MMAs [z_hi | z_lo | 1 1 0..] . [U ; U ; b_hi ; b_lo ; 0..]
+//               the filter MMAs [z_hi | z_lo | 1] . [U ; U ; b_hi + b_lo]
 //   warps 2..17 epilogue: at a token tile's start they read z from TMEM and
 //               write it as bf16 into the z tile; per unit, as the low-rank
 //               forward: the accumulator row of a token times its x window,
@@ -54,7 +56,7 @@ struct Params {
     int rp;                        // R rounded up to 16: MMA N of the z product, K of the filter product
     int n_nb, n_mt, n_units, n_zitems;  // channel blocks, token tiles, units, z items per token tile
     unsigned ublk;                 // bytes of one 64-column block of a unit item's U rows: (rp + 16) rows x 128 B
-    unsigned zt_off, y_off, ring_off, slot_bytes, x_in_slot, w1_in_slot;
+    unsigned zt_off, one_off, y_off, ring_off, slot_bytes, x_in_slot, w1_in_slot;
     unsigned u_bytes, x_bytes, z_item_bytes;  // TMA bytes of a unit item's U rows and x tile, of a z item
     int nslots;
     int *status;
@@ -106,7 +108,8 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
     Header *hdr = reinterpret_cast<Header *>(smem_raw);
     uint8_t *base = smem_raw + 1024;
     base += (1024u - (smem_u32(base) & 1023u)) & 1023u;
-    uint8_t *zt = base + p.zt_off;       // z tile: [128 tokens][2 rp + 16] bf16, K-major, 64-column chunks of 16 KB
+    uint8_t *zt = base + p.zt_off;       // z tile: [128 tokens][2 rp] bf16, K-major, 64-column chunks of 16 KB
+    uint8_t *one_s = base + p.one_off;   // all-ones A tile [128 rows][16 K], no swizzle: meets the bias rows
     uint8_t *y_s = base + p.y_off;       // per working epilogue warp: [32 rows][YB] staging for its own stores
     uint8_t *ring = base + p.ring_off;   // nslots slots of slot_bytes
 
@@ -126,13 +129,8 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
         hdr->abort_flag = 0;
         fence_mbarrier_init();
     }
-    // the z tile's last K step: columns 2rp, 2rp+1 hold 1.0 (they meet the bias hi and lo rows of U), the rest 0
-    for (int t = threadIdx.x; t < kM * 2; t += blockDim.x) {
-        const int row = t >> 1, half = t & 1;
-        const int kc = 2 * p.rp + 8 * half;  // 16-byte chunk holding columns kc .. kc+7
-        uint4 v = make_uint4(half ? 0u : 0x3F803F80u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(zt + (kc >> 6) * 16384 + row * 128 + ((((kc & 63) >> 3) ^ (row & 7)) << 4)) = v;
-    }
+    for (int i = threadIdx.x; i < kM * 16 / 2; i += blockDim.x)
+        reinterpret_cast<uint32_t *>(one_s)[i] = 0x3F803F80u;  // bf16 1.0 pairs
     fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(&hdr->tmem_base, kTmemCols);
@@ -148,10 +146,8 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
     const uint32_t tmem = hdr->tmem_base;
     volatile int *abort_flag = &hdr->abort_flag;
 
-    // this CTA's token tiles [m_begin, m_end), every channel block of each
-    const int m_begin = static_cast<int>(static_cast<long long>(blockIdx.x) * p.n_mt / gridDim.x);
-    const int m_end = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.n_mt / gridDim.x);
-    const int u_begin = m_begin * p.n_nb, u_end = m_end * p.n_nb;
+    const int u_begin = static_cast<int>(static_cast<long long>(blockIdx.x) * p.n_units / gridDim.x);
+    const int u_end = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.n_units / gridDim.x);
 
     int issued_last[kMaxSlots];  // producer: last item index loaded into each slot
 #pragma unroll
@@ -164,6 +160,17 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
         int item = 0;
         int cur_mt = -1;
         bool ok = true;
+        // x is read once: its lines may leave L2 first
+        const uint64_t pol_once = l2_policy_evict_first();
+        float bv[8];  // this lane's 8 bias columns (chunk `lane`) of the next unit item's block
+        auto load_bias = [&](int nbx) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int gn = nbx * NB + lane * 8 + e;
+                bv[e] = (lane < NB / 8 && gn < p.N) ? __ldg(p.bias + gn) : 0.f;
+            }
+        };
+        if (u_begin < u_end) load_bias(u_begin % p.n_nb);
         for (int v = u_begin; v < u_end && ok; ++v) {
             const int mt = v / p.n_nb, nb = v - mt * p.n_nb;
             if (mt != cur_mt) {
@@ -188,30 +195,27 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
             if (!ok) break;
             uint8_t *sl = ring + rs.s * p.slot_bytes;
             // the bias rows rp .. rp+15 of each 64-column block (128-byte swizzled, MN-major like the U rows):
-            // row rp = bf16(b), row rp+1 = bf16(b - bf16(b)), the rest zero
-            for (int q = lane; q < (NB / 8) * 16; q += 32) {
-                const int r = q / (NB / 8), cc = q - r * (NB / 8);  // K row offset, 8-column chunk of the block
-                const int blk = cc >> 3, c8 = cc & 7;
-                uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
-                if (r < 2) {
-                    uint32_t w[4];
+            // row rp = bf16(b), row rp+1 = bf16(b - bf16(b)) from this lane's 8 columns, the rest zero
+            if (lane < NB / 8) {
+                uint32_t whi[4], wlo[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t hv[2];
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int gn = nb * NB + cc * 8 + 2 * e + hh;
-                            const float b = gn < p.N ? __ldg(p.bias + gn) : 0.f;
-                            const float bh = __bfloat162float(__float2bfloat16_rn(b));
-                            hv[hh] = static_cast<uint32_t>(
-                                __bfloat16_as_ushort(__float2bfloat16_rn(r == 0 ? b : b - bh)));
-                        }
-                        w[e] = hv[0] | (hv[1] << 16);
-                    }
-                    v4 = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 4; ++e) {
+                    __nv_bfloat162 hv = __float22bfloat162_rn(make_float2(bv[2 * e], bv[2 * e + 1]));
+                    __nv_bfloat162 lv = __float22bfloat162_rn(
+                        make_float2(bv[2 * e] - __low2float(hv), bv[2 * e + 1] - __high2float(hv)));
+                    whi[e] = *reinterpret_cast<uint32_t *>(&hv);
+                    wlo[e] = *reinterpret_cast<uint32_t *>(&lv);
                 }
-                const int kr = p.rp + r;
-                *reinterpret_cast<uint4 *>(sl + blk * p.ublk + kr * 128 + ((c8 ^ (kr & 7)) << 4)) = v4;
+                const int blk = lane >> 3, c8 = lane & 7;
+                *reinterpret_cast<uint4 *>(sl + blk * p.ublk + p.rp * 128 + ((c8 ^ (p.rp & 7)) << 4)) =
+                    make_uint4(whi[0], whi[1], whi[2], whi[3]);
+                *reinterpret_cast<uint4 *>(sl + blk * p.ublk + (p.rp + 1) * 128 + ((c8 ^ ((p.rp + 1) & 7)) << 4)) =
+                    make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+            }
+            for (int q = lane; q < (NB / 8) * 14; q += 32) {
+                const int kr = p.rp + 2 + q / (NB / 8), cc = q % (NB / 8);
+                *reinterpret_cast<uint4 *>(sl + (cc >> 3) * p.ublk + kr * 128 + (((cc & 7) ^ (kr & 7)) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -219,11 +223,12 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
                 mbar_arrive_expect_tx(&hdr->full[rs.s], p.u_bytes + p.x_bytes);
                 for (int blk = 0; blk < NBLK; ++blk)
                     tma_load_2d(sl + blk * p.ublk, &tm_u, &hdr->full[rs.s], nb * NB + blk * 64, 0);
-                tma_load_2d(sl + p.x_in_slot, &tm_x, &hdr->full[rs.s], nb * CB, mt * kM - (W - 1));
+                tma_load_2d_hint(sl + p.x_in_slot, &tm_x, &hdr->full[rs.s], nb * CB, mt * kM - (W - 1), pol_once);
                 issued_last[rs.s] = item;
             }
             ++item;
             rs.step(p.nslots);
+            if (v + 1 < u_end) load_bias((v + 1) % p.n_nb);  // the next item's bias, loaded while this one flies
         }
         if (!ok && lane == 0) lr_abort(p.status, abort_flag);
     } else if (warp == 1) {
@@ -274,16 +279,17 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) {
-                // [z_hi | z_lo | 1 1 0 ..] . [U ; U ; b_hi ; b_lo ; 0 ..]: rp/16 K steps of each half of the code
-                // against the same U rows, then one of the bias
+                // [z_hi | z_lo] . [U ; U]: rp/16 K steps of each half of the code against the same U rows; then
+                // ones . [b_hi ; b_lo ; 0 ..], the bias rows after the U rows
                 const uint32_t sl = smem_u32(ring + rs.s * p.slot_bytes);
                 const uint32_t zs = smem_u32(zt);
                 const int nks = p.rp / 16;
-                for (int ks = 0; ks <= 2 * nks; ++ks) {
-                    const int ur = ks < nks ? ks : ks < 2 * nks ? ks - nks : nks;  // K step of the U rows
+                for (int ks = 0; ks < 2 * nks; ++ks)
                     umma_bf16(tmem + b * 256, sdesc_kmajor_sw128(zs + (ks >> 2) * 16384 + (ks & 3) * 32),
-                              sdesc(sl + ur * 2048, p.ublk, 1024, 2), IDESC_F, ks > 0 ? 1u : 0u);
-                }
+                              sdesc(sl + (ks < nks ? ks : ks - nks) * 2048, p.ublk, 1024, 2), IDESC_F,
+                              ks > 0 ? 1u : 0u);
+                umma_bf16(tmem + b * 256, sdesc(smem_u32(one_s), 128, 256, 0), sdesc(sl + nks * 2048, p.ublk, 1024, 2),
+                          IDESC_F, 1u);
                 umma_commit(&hdr->empty[rs.s]);
                 umma_commit(&hdr->tmem_full[b]);
                 mma_issued = true;
@@ -479,9 +485,10 @@ static dsc_status launch_zfwd(const LowrankZArgs &a, const DeviceInfo &dev)
     p.u_bytes = NBLK * p.rp * 128;
     p.x_bytes = XR * RB;
     p.z_item_bytes = 2 * 16384 + 2 * p.rp * 128;
-    // shared memory: [header 1 KB][align slack 1 KB][z tile][y staging][ring]
+    // shared memory: [header 1 KB][align slack 1 KB][z tile][ones tile][y staging][ring]
     p.zt_off = 0;
-    unsigned off = ((2 * p.rp + 16 + 63) / 64) * 16384;
+    p.one_off = ((2 * p.rp + 63) / 64) * 16384;
+    unsigned off = p.one_off + kM * 32;
     p.y_off = align_up(off, 1024);
     off = p.y_off + kEpiWarps * 32 * (RB / NCW);
     p.ring_off = align_up(off, 1024);
@@ -509,7 +516,7 @@ static dsc_status launch_zfwd(const LowrankZArgs &a, const DeviceInfo &dev)
     auto kern = lowrank_zfwd_tc<W, CB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return DSC_ERR_CUDA;
-    const int grid = dev.sm_count < p.n_mt ? dev.sm_count : p.n_mt;
+    const int grid = dev.sm_count < p.n_units ? dev.sm_count : p.n_units;
     return launch_overlapped(kern, grid, kThreads, smem, a.stream, tm_h, tm_w1, tm_u, tm_x, tm_y, p);
 }
 
