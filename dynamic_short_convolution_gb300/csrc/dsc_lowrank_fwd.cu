@@ -11,7 +11,8 @@
 // U block (TMA, 128-byte swizzle, read as an MN-major operand) stays resident
 // in shared memory while the CTA streams over token tiles.
 //   warp 0      TMA producer: z tile (K-major, swizzled) and the x tile with
-//               its (W-1)-token causal halo; per-token valid-tap counts
+//               its (W-1)-token causal halo; the tile's per-token valid-tap
+//               counts, written beside the x tile while the loads fly
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma (M=128, N=NB, K=16 per
 //               instruction) into one of two TMEM accumulators
 //   warps 2..17 epilogue: tcgen05.ld of the accumulator row of one token,
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
 
     if (warp == 0) {
         // ---------------- producer: streams z and x tiles from the first cycle, across block changes
+        DocCursor cursor;  // lane l: tokens l, l+32, l+64, l+96 of each tile, increasing within a block
         int i = 0;
         int s = 0;                                  // stage and its phase: stepped, not divided, per tile
         uint32_t ph = 0;
@@ -154,6 +156,15 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             }
             const int t0 = mt * kM;
             uint8_t *st = stages + s * p.stage_bytes;
+            // valid taps of the tile's tokens (the slot is free: the epilogue read the previous ones first)
+            if (mt == 0 || v == u_begin) cursor.reset();
+            int8_t *nvs = reinterpret_cast<int8_t *>(st + p.nv_off_in_stage);
+#pragma unroll
+            for (int r = 0; r < kM; r += 32) {
+                const int t = t0 + r + lane;
+                nvs[r + lane] = static_cast<int8_t>(t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W);
+            }
+            __syncwarp();
             if (lane == 0) {
                 mbar_arrive_expect_tx(&hdr->full[s], p.z_bytes + p.x_bytes);
                 for (int a = 0; a < p.kchunks; ++a) tma_load_2d(st + a * 16384, &tm_z, &hdr->full[s], a * 64, t0);
@@ -261,7 +272,6 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         const int h = (warp - kEpiWarp0) >> 2;           // which share of the channel groups
         const int row = q * 32 + lane;                   // token within the tile
         uint8_t *ywarp = y_s + (warp - kEpiWarp0) * (2 * 32 * YB);
-        DocCursor cursor;  // this thread's token increases from tile to tile within a block
         int i = 0;
         int s = 0;
         uint32_t ph = 0;
@@ -269,13 +279,8 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
         for (int v = u_begin; v < u_end;
              ++v, ++i, s = (s + 1 == p.nstages) ? 0 : s + 1, ph ^= (s == 0), mt = (mt + 1 == p.n_mt) ? 0 : mt + 1,
                  nb += (mt == 0)) {
-            if (mt == 0) cursor.reset();  // a new block starts again from the first token
             const int b = i & 1;
             const uint32_t tph = (i >> 1) & 1;
-            // valid taps of this token, worked out while the tile's accumulator is still being computed
-            const int t = mt * kM + row;
-            const int nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;  // valid taps of this token
-            const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
             bool ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[s], ph, p.wait_ns);
             // the other roles' failures reach this warp through the barriers it waits on
             ok = __all_sync(0xffffffffu, ok);
@@ -289,6 +294,8 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
             tc_fence_after();
             const uint8_t *st = stages + s * p.stage_bytes;
             const uint8_t *xs = st + p.x_off_in_stage;
+            const int nv = reinterpret_cast<const int8_t *>(st + p.nv_off_in_stage)[row];  // valid taps of this token
+            const bool full_taps = __all_sync(0xffffffffu, nv == W);  // no token of this warp near a document start
             uint8_t *ys = ywarp + b * (32 * YB);
             bool ys_free = false;  // this warp's store from two tiles ago has left buffer b
             const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * 256;

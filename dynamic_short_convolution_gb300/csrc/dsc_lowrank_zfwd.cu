@@ -325,6 +325,8 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         uint8_t *ys = y_s + (warp - kEpiWarp0) * (32 * YB);
         DocCursor cursor;
+        int nv = W, nv_mt = -1;  // valid taps of this thread's token in tile nv_mt
+        bool full_taps = true;
         RingPos rs;
         int cur_mt = -1;
         uint32_t zc = 0;
@@ -377,9 +379,12 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
                 if (lane == 0) mbar_arrive(&hdr->z_ready);
                 cur_mt = mt;
             }
-            const int t = mt * kM + row;
-            const int nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;
-            const bool full_taps = __all_sync(0xffffffffu, nv == W);
+            if (mt != nv_mt) {  // this thread's token, hence its valid taps, changes only with the tile
+                const int t = mt * kM + row;
+                nv = t < p.BT ? cursor.taps(t, p.T, W, p.cu, p.n_docs) : W;
+                full_taps = __all_sync(0xffffffffu, nv == W);
+                nv_mt = mt;
+            }
             ok = mbar_wait(&hdr->tmem_full[b], tph, p.wait_ns) && mbar_wait(&hdr->full[rs.s], rs.ph, p.wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
