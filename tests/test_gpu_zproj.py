@@ -45,6 +45,8 @@ CASES = [
     (1, 180, 128, 2048, 4, 64, True),   # the model width of the 2B-scale layer input
     (2, 150, 104, 64, 6, 80, True),     # D not a multiple of the channel block
     (1, 150, 128, 64, 8, 128, True),    # the largest rank at the widest filter: 16-channel blocks
+    (1, 5, 8, 8, 2, 8, False),          # one partial token tile, one partial channel block, one partial K chunk
+    (2, 60, 24, 16, 3, 16, True),       # D and Dm far below a block, documents shorter than W
 ]
 
 
