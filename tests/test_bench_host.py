@@ -1,9 +1,13 @@
 """Host logic of bench.py that needs no GPU: the DRAM traffic of a kernel is reported only while its
 sources are the ones the committed ncu counters were taken on, the recorded figures are self-consistent,
-and the whole-job throughput counts every replica's tokens."""
+and the whole-job throughput counts every replica's tokens; the CPU-baseline sample runs for every
+workload kind."""
 import os
 import re
 import sys
+from dataclasses import replace
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
@@ -55,3 +59,30 @@ def test_peaks_fall_back_to_the_stated_figures_without_the_measured_file(tmp_pat
     assert bench.peaks() == (6800.0, 1900.0, 1700.0, "fallback")
     (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6783.1, "bf16_tflops": 1883.2}')
     assert bench.peaks() == (6783.1, 1883.2, 1883.2, "measured")
+
+
+ALL_WORKLOADS = ["tiny_fp32", "headwise_bf16", "material_bf16", "lowrank_bf16", "qkv_packed_bf16", "static_bf16",
+                 "decode_bf16", "proj_qkv_bf16", "lowrank_zproj_bf16"]
+
+
+def test_the_list_names_every_workload():
+    from dynamic_short_convolution_gb300 import inputs
+
+    assert sorted(ALL_WORKLOADS) == sorted(w.name for w in inputs.WORKLOADS.values())
+
+
+@pytest.mark.parametrize("name", ALL_WORKLOADS)
+def test_cpu_baseline_step_runs_for_every_workload(name):
+    """The CPU-baseline sample (bench's oracle step) runs on every workload kind, on a few tokens of a
+    shortened copy, so the reference arm and the per-row CPU figures cannot fail on the GPU machine."""
+    import bench
+    import oracle
+    from dynamic_short_convolution_gb300 import inputs
+
+    wl = inputs.by_name(name)
+    if wl.kind != "decode":
+        wl = inputs.shrink(replace(wl, B=1), 16)
+    else:
+        wl = replace(wl, B=4)
+    d = inputs.make(wl)
+    bench._oracle_step(oracle, wl, d, 0, 2)
