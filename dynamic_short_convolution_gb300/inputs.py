@@ -27,8 +27,8 @@ for real activations):
   (so w = h Wg^T + bg has variance about 0.1, as in ``qkv_packed_bf16``)
 * ``lowrank_zproj_bf16`` the ``lowrank_bf16`` shape (B=8 T=2048 D=2048 W=4 R=64) with the
   generator's code z computed from the layer input: h [B, T, Dm=2048] ~N(0,1) and the
-  first projection W1 [R, Dm] ~N(0, 1/Dm) (so z = h W1^T ~N(0,1), as in ``lowrank_bf16``);
-  x, U and bias as there
+  first projection W1 [R, Dm] ~N(0, 1/Dm) and its bias b1 [R] ~N(0, 0.01) fp32 (so
+  z = h W1^T + b1 has variance about 1, as in ``lowrank_bf16``); x, U and bias as there
 * ``decode_bf16``   B=512 sequences, one new token each, D=6144 (Q, K and V of a
   2048-wide model side by side), W=4 H=16 bf16; history ring [B, W-1, D] ~N(0,1),
   positions ~U{0..4095} (a fifth of them below W-1, where the document's history
@@ -39,7 +39,7 @@ Values are drawn in fp32 and rounded to nearest-even bf16 where the workload
 is bf16.  Seeds: 1000 * workload id + tensor index (x=0, w=1, dy=2, z=3, U=4,
 bias=5, document lengths=6, decode history=7, decode positions=8, projection input h=0,
 Q/K/V weights=9, generator weights=10, generator bias=5; for the low-rank code's projection:
-layer input h=11, first projection W1=12).
+layer input h=11, first projection W1=12, its bias b1=13).
 """
 from __future__ import annotations
 
@@ -48,7 +48,7 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-X, WGT, DY, Z, U, BIAS, LENS, HIST, POS, PWX, PWG, ZH, ZW1 = range(13)
+X, WGT, DY, Z, U, BIAS, LENS, HIST, POS, PWX, PWG, ZH, ZW1, ZB1 = range(14)
 
 
 @dataclass(frozen=True)
@@ -150,6 +150,7 @@ def make(wl: Workload, with_grad: bool = True) -> dict:
         Dm = int(wl.extra["Dm"])
         out["h"] = _normal((wl.B, wl.T, Dm), 1.0, wl.wid, ZH, dt)
         out["W1"] = _normal((wl.R, Dm), 1.0 / math.sqrt(Dm), wl.wid, ZW1, dt)
+        out["b1"] = _normal((wl.R,), 0.1, wl.wid, ZB1, torch.float32)
         out["U"] = _normal((wl.R, wl.D * wl.W), 1.0 / math.sqrt(wl.R), wl.wid, U, dt)
         out["bias"] = _normal((wl.D * wl.W,), 0.1, wl.wid, BIAS, torch.float32)
         out["cu_seqlens"] = doc_offsets(wl)
@@ -240,7 +241,7 @@ def custom_proj(B, T, Dm, D, W, H=1, seed_id=500, w_std=0.5, packed=False, doc_m
 
 
 def custom_zproj(B, T, Dm, D, W, R, seed_id=700, packed=False, doc_min=1, doc_max=None) -> Workload:
-    """A low-rank workload whose code z = h W1^T is computed from the layer input h [B, T, Dm] (seeded by
+    """A low-rank workload whose code z = h W1^T + b1 is computed from the layer input h [B, T, Dm] (seeded by
     ``seed_id``)."""
     return Workload(seed_id, "custom_zproj", "zproj", B, T, D, W, R=R, packed=packed, doc_min=doc_min,
                     doc_max=doc_max if doc_max is not None else T, extra={"Dm": Dm})

@@ -20,7 +20,7 @@ section "Key design 1"):
 * ``decode_step``: y of one new token per sequence against a history ring (eq. 2 + eq. 3, one step)
 * ``proj_fwd``:    y of eq. 2 + 3 with x = h Wx^T and w = h Wg^T + bg computed from the projection's input
                    h ("Placement": the generator's projection beside the Q/K/V projection)
-* ``lowrank_zproj_fwd``: the low-rank form with its code z = h W1^T computed from the layer input h
+* ``lowrank_zproj_fwd``: the low-rank form with its code z = h W1^T + b1 computed from the layer input h
                    ("Parameterization": the generator maps D -> R -> W*D)
 
 Every function takes tensors laid out exactly like the CUDA library's
@@ -86,8 +86,8 @@ def _load():
             lib.dsco_static_bwd.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, i64, i64, vp, vp]
             lib.dsco_decode_step.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i64, vp]
             lib.dsco_proj_fwd_rows.argtypes = [vp, vp, vp, vp, i32, i32, i64, i64, i64, i32, i64, vp, i64, i64, vp]
-            lib.dsco_lowrank_zproj_fwd_rows.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i64, i64, i32, i64, vp,
-                                                         i64, i64, vp]
+            lib.dsco_lowrank_zproj_fwd_rows.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i64, i64, i64, i32, i64,
+                                                         vp, i64, i64, vp]
             _lib = lib
     return _lib
 
@@ -197,9 +197,9 @@ def lowrank_fwd(x, z, U, bias, W: int, cu_seqlens=None, rows=None) -> np.ndarray
     return y
 
 
-def lowrank_zproj_fwd(x, h, W1, U, bias, W: int, cu_seqlens=None, rows=None) -> np.ndarray:
-    """Low-rank form with the generator's first projection: z = h W1^T (h [B, T, Dm], W1 [R, Dm]), then the
-    filter z U + bias and eq. 2 + 3 on x.  y rows [r0, r1), float64 [r1-r0, D]."""
+def lowrank_zproj_fwd(x, h, W1, U, bias, W: int, cu_seqlens=None, rows=None, b1=None) -> np.ndarray:
+    """Low-rank form with the generator's first projection: z = h W1^T + b1 (h [B, T, Dm], W1 [R, Dm], b1 [R]
+    or None), then the filter z U + bias and eq. 2 + 3 on x.  y rows [r0, r1), float64 [r1-r0, D]."""
     B, T, D = x.shape
     Dm = h.shape[-1]
     R = W1.shape[0]
@@ -211,12 +211,18 @@ def lowrank_zproj_fwd(x, h, W1, U, bias, W: int, cu_seqlens=None, rows=None) -> 
     p1, c1, k1 = _raw(W1)
     pu, cu_, ku = _raw(U)
     pb, cb, kb = _bias_ptr(bias)
+    if b1 is None:
+        pz, kz = None, None
+    else:
+        assert tuple(b1.shape) == (R,)
+        b1 = b1.to(bias.dtype)  # one storage type for both biases
+        pz, _, kz = _bias_ptr(b1)
     dt = _same_dtype(cx, ch, c1, cu_)
     ds = docstarts(B, T, cu_seqlens)
     r0, r1 = _rows(rows, BT)
     y = np.empty((r1 - r0, D), dtype=np.float64)
-    _load().dsco_lowrank_zproj_fwd_rows(px, ph, p1, pu, pb, cb, dt, BT, Dm, D, W, R, _ptr(ds), r0, r1, _ptr(y))
-    del kx, kh, k1, ku, kb
+    _load().dsco_lowrank_zproj_fwd_rows(px, ph, p1, pz, pu, pb, cb, dt, BT, Dm, D, W, R, _ptr(ds), r0, r1, _ptr(y))
+    del kx, kh, k1, ku, kb, kz
     return y
 
 

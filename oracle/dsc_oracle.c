@@ -184,15 +184,15 @@ void dsco_lowrank_fwd_rows(const void *x, const void *z, const void *U, const vo
  * Low-rank forward with the generator's first projection ("Parameterization":
  * the generator maps the layer input through D -> R -> W*D; "Placement": its
  * first projection runs beside the Q/K/V projection): rows [r0, r1) of
- *   z[t, r]  = sum_i h[t, i] W1[r, i]                    (the rank-R code)
+ *   z[t, r]  = b1[r] + sum_i h[t, i] W1[r, i]            (the rank-R code; b1 may be NULL: no bias)
  *   Wt[t, n] = sum_r z[t, r] U[r, n] + bias[n]            n = d*W + k
  *   y[t, d]  = x[t, d] + sum_k Wt[t, d*W+k] * x~[t-k, d]
  * all in fp64.  h [BT, Dm], W1 [R, Dm], x [BT, D], U [R, D*W] share one
- * storage type; bias has its own (bdt).
+ * storage type; bias and b1 have their own (bdt).
  */
-void dsco_lowrank_zproj_fwd_rows(const void *x, const void *h, const void *W1, const void *U, const void *bias, int bdt,
-                                 int dt, int64_t BT, int64_t Dm, int64_t D, int W, int64_t R, const int64_t *ds,
-                                 int64_t r0, int64_t r1, double *y)
+void dsco_lowrank_zproj_fwd_rows(const void *x, const void *h, const void *W1, const void *b1, const void *U,
+                                 const void *bias, int bdt, int dt, int64_t BT, int64_t Dm, int64_t D, int W, int64_t R,
+                                 const int64_t *ds, int64_t r0, int64_t r1, double *y)
 {
     const int64_t NW = D * W;
     (void)BT;
@@ -203,7 +203,7 @@ void dsco_lowrank_zproj_fwd_rows(const void *x, const void *h, const void *W1, c
 #pragma omp for schedule(static)
         for (int64_t t = r0; t < r1; ++t) {
             for (int64_t r = 0; r < R; ++r) {
-                double acc = 0.0;
+                double acc = b1 ? load(b1, bdt, r) : 0.0;
                 for (int64_t i = 0; i < Dm; ++i) acc += load(h, dt, t * Dm + i) * load(W1, dt, r * Dm + i);
                 zr[r] = acc;
             }
