@@ -434,7 +434,7 @@ class ZprojProblem:
     """The low-rank forward with the generator's first projection on chip (forward only): x, the layer input
     h and the weights in, y out.  Algorithmic bytes: x, h, W1, U and the bias read once, y written once;
     flops: the two projections, 2 B T R (Dm + D W).  ``unfused`` is the caller's path without the fused kernel:
-    z = h W1^T by cuBLAS, stored bf16, then dsc_lowrank_fwd."""
+    z = h W1^T + b1 by cuBLAS, stored bf16, then dsc_lowrank_fwd."""
 
     def __init__(self, wl, dev):
         import torch
@@ -447,14 +447,16 @@ class ZprojProblem:
         BT = wl.B * wl.T
         Dm = g["h"].shape[-1]
         self.Dm = Dm
-        t = {"x": g["x"], "h": g["h"], "W1": g["W1"], "U": g["U"], "bias": g["bias"], "cu": g["cu_seqlens"],
+        t = {"x": g["x"], "h": g["h"], "W1": g["W1"], "b1": g["b1"], "U": g["U"], "bias": g["bias"], "cu": g["cu_seqlens"],
              "y": torch.empty(wl.B, wl.T, wl.D, dtype=torch.bfloat16, device=dev),
              "z": torch.empty(wl.B, wl.T, wl.R, dtype=torch.bfloat16, device=dev)}
         per = (g["x"].numel() + g["h"].numel()) * 2
-        self.bytes_fwd = per + (g["W1"].numel() + g["U"].numel()) * 2 + 4 * g["bias"].numel() + BT * wl.D * 2
+        self.bytes_fwd = (per + (g["W1"].numel() + g["U"].numel()) * 2 + 4 * (g["bias"].numel() + g["b1"].numel())
+                          + BT * wl.D * 2)
         self.bytes_bwd = 0
         self.flops_fwd = 2 * BT * wl.R * (Dm + wl.D * wl.W)
         self.flops_bwd = 0
+        self.b1_16 = g["b1"].to(torch.bfloat16)
         self.rot = _Sets({"x": t["x"], "h": t["h"]}, per)
         self.t = t
         self.cur = t
@@ -466,7 +468,7 @@ class ZprojProblem:
         import dynamic_short_convolution_gb300 as dsc
 
         c = self.cur
-        dsc.dsc_lowrank_zproj_fwd(c["x"], c["h"], c["W1"], c["U"], c["bias"], c["y"], cu_seqlens=c["cu"])
+        dsc.dsc_lowrank_zproj_fwd(c["x"], c["h"], c["W1"], c["U"], c["bias"], c["y"], b1=c["b1"], cu_seqlens=c["cu"])
 
     def unfused(self, ev=None):
         import torch
@@ -474,7 +476,7 @@ class ZprojProblem:
         import dynamic_short_convolution_gb300 as dsc
 
         c = self.cur
-        torch.matmul(c["h"].view(-1, self.Dm), c["W1"].t(), out=c["z"].view(-1, self.wl.R))
+        torch.addmm(self.b1_16, c["h"].view(-1, self.Dm), c["W1"].t(), out=c["z"].view(-1, self.wl.R))
         if ev:
             ev[0].record()
         dsc.dsc_lowrank_fwd(c["x"], c["z"], c["U"], c["bias"], c["y"], cu_seqlens=c["cu"])
@@ -607,7 +609,7 @@ def _oracle_step(oracle, wl, d, r0, r1):
         oracle.proj_fwd(d["h"], d["Wx"], d["Wg"], d["bg"], wl.W, wl.H, cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
     elif wl.kind == "zproj":  # the low-rank forward with z from the layer input: rows [r0, r1) (no backward)
         oracle.lowrank_zproj_fwd(d["x"], d["h"], d["W1"], d["U"], d["bias"], wl.W, cu_seqlens=d["cu_seqlens"],
-                                 rows=(r0, r1))
+                                 rows=(r0, r1), b1=d["b1"])
     elif wl.kind == "decode":  # one decode step of sequences [r0, r1) (no backward: inference)
         oracle.decode_step(d["x"][r0:r1], d["w"][r0:r1], d["hist"][r0:r1], d["pos"][r0:r1], wl.W, wl.H)
     else:
@@ -1000,7 +1002,7 @@ def measure_zproj_row(prob, hbm_peak, tc_peak, reps=30):
             "roofline_frac": 1e6 * bound / (1e3 * mf), "unfused_us": 1e3 * mu,
             "unfused_gemm_z_us": 1e3 * statistics.median(gz),
             "unfused_conv_us": 1e3 * (mu - statistics.median(gz)), "speedup_vs_unfused": mu / mf,
-            "unfused_path": "torch.matmul (cuBLAS) for z = h W1^T stored bf16, then dsc_lowrank_fwd",
+            "unfused_path": "torch.addmm (cuBLAS) for z = h W1^T + b1 stored bf16, then dsc_lowrank_fwd",
             "timing": f"median of {reps} calls, CUDA events, x and h rotated over copies larger than L2"}
 
 

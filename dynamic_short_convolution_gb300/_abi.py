@@ -31,7 +31,7 @@ SIGNATURES = {
     "dsc_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "dsc_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "dsc_lowrank_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
-    "dsc_lowrank_zproj_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "dsc_lowrank_zproj_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "dsc_lowrank_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "dsc_lowrank_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i,
                              _vp]),
@@ -195,9 +195,9 @@ def dsc_lowrank_fwd(x, z, U, bias, y=None, *, cu_seqlens=None, stream=None):
     return y
 
 
-def dsc_lowrank_zproj_fwd(x, h, W1, U, bias, y=None, *, cu_seqlens=None, stream=None):
-    """y = x + dynamic conv(x) with the code z = h W1^T and the filter z U + bias formed on chip: x [B,T,D],
-    h [B,T,Dm], W1 [R,Dm], U [R,D*W], bias [D*W] fp32."""
+def dsc_lowrank_zproj_fwd(x, h, W1, U, bias, y=None, *, b1=None, cu_seqlens=None, stream=None):
+    """y = x + dynamic conv(x) with the code z = h W1^T + b1 and the filter z U + bias formed on chip: x [B,T,D],
+    h [B,T,Dm], W1 [R,Dm], b1 [R] fp32 or None, U [R,D*W], bias [D*W] fp32."""
     dev = _lead(x, "x", 3)
     B, T, D = x.shape
     if not isinstance(h, torch.Tensor) or h.dim() != 3 or tuple(h.shape[:2]) != (B, T):
@@ -212,9 +212,10 @@ def dsc_lowrank_zproj_fwd(x, h, W1, U, bias, y=None, *, cu_seqlens=None, stream=
     if not isinstance(bias, torch.Tensor) or tuple(bias.shape) != (D * W,):
         raise ValueError("bias must be [D*W]")
     y = torch.empty_like(x) if y is None else y
+    b1p = None if b1 is None else _dev(b1, "b1", torch.float32, (R,), dev)
     cu, n = _cu(cu_seqlens, dev)
     s = lib().dsc_lowrank_zproj_fwd(_dev(x, "x"), _dev(h, "h", x.dtype, device=dev), _dev(W1, "W1", x.dtype, device=dev),
-                                    _dev(U, "U", x.dtype, device=dev), _dev(bias, "bias", torch.float32, device=dev),
+                                    b1p, _dev(U, "U", x.dtype, device=dev), _dev(bias, "bias", torch.float32, device=dev),
                                     _dev(y, "y", x.dtype, x.shape, dev), B, T, D, Dm, W, R, _dt(x), cu, n,
                                     _stream(stream))
     _check(s, "dsc_lowrank_zproj_fwd")

@@ -248,20 +248,21 @@ dsc_status dsc_lowrank_fwd(const void *x, const void *z, const void *U, const fl
     return lowrank_fwd(a);
 }
 
-dsc_status dsc_lowrank_zproj_fwd(const void *x, const void *h, const void *W1, const void *U, const float *bias,
-                                 void *y, int B, int T, int D, int Dm, int W, int R, dsc_dtype dt,
+dsc_status dsc_lowrank_zproj_fwd(const void *x, const void *h, const void *W1, const float *b1, const void *U,
+                                 const float *bias, void *y, int B, int T, int D, int Dm, int W, int R, dsc_dtype dt,
                                  const int32_t *cu_seqlens, int n_docs, cudaStream_t stream)
 {
     // x, U, bias and the shape as for dsc_lowrank_fwd (h stands in for z in the pointer checks)
     dsc_status s = lowrank_check(x, h, U, bias, B, T, D, W, R, dt, cu_seqlens, n_docs);
     if (s != DSC_OK) return s;
     if (!W1 || !y || Dm < 1) return DSC_ERR_INVALID_ARG;
+    if (b1 != nullptr && !elem_aligned(b1, 4)) return DSC_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * T * Dm >= (1LL << 31) || static_cast<long long>(R) * Dm >= (1LL << 31))
         return DSC_ERR_INVALID_ARG;
     if (Dm % 8 != 0 || R > 128) return DSC_ERR_UNSUPPORTED;
     if (!aligned16(W1) || !aligned16(y)) return DSC_ERR_UNSUPPORTED;
     LowrankZArgs a;
-    a.x = x; a.h = h; a.W1 = W1; a.U = U; a.bias = bias; a.y = y;
+    a.x = x; a.h = h; a.W1 = W1; a.b1 = b1; a.U = U; a.bias = bias; a.y = y;
     a.B = B; a.T = T; a.D = D; a.Dm = Dm; a.W = W; a.R = R;
     a.cu = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0; a.stream = stream;
     return lowrank_zproj_fwd(a);

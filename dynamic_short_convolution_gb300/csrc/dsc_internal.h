@@ -91,6 +91,7 @@ struct LowrankZArgs {
     const void *x = nullptr;
     const void *h = nullptr;
     const void *W1 = nullptr;
+    const float *b1 = nullptr;  // may be null
     const void *U = nullptr;
     const float *bias = nullptr;
     void *y = nullptr;

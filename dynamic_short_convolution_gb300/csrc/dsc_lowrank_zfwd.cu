@@ -4,7 +4,7 @@
 // D -> R -> W*D; "Placement": its first projection runs beside the Q/K/V
 // projection; "Efficient training": the generated filter never reaches HBM):
 //
-//   z[t, r]      = sum_i h[t, i] W1[r, i]                       (tensor cores, per token tile)
+//   z[t, r]      = sum_i h[t, i] W1[r, i] + b1[r]               (tensor cores, per token tile)
 //   Wt[t, d*W+k] = sum_r z[t, r] U[r, d*W+k] + bias[d*W+k]       (tensor cores, per unit)
 //   y[t, d]      = x[t, d] + sum_k Wt[t, d*W+k] * x~[t-k, d]      (epilogue)
 //
@@ -68,6 +68,7 @@ constexpr int kMaxSlots = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
 
 struct Params {
+    const float *b1;               // the first projection's bias [R], or null
     const float *bias;
     const int32_t *cu;
     int n_docs;
@@ -353,11 +354,15 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
                 for (int g = h; g < p.rp / 8; g += NCW) {
                     uint32_t zr[8];
                     tmem_ld_x8(tmem + lane_off + b * 256 + g * 8, zr);
+                    float b1v[8];  // the first projection's bias of these 8 columns (none past R)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) b1v[e] = (p.b1 != nullptr && g * 8 + e < p.R) ? __ldg(p.b1 + g * 8 + e) : 0.f;
                     tmem_ld_wait();
                     uint32_t whi[4], wlo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float z0 = __uint_as_float(zr[2 * e]), z1 = __uint_as_float(zr[2 * e + 1]);
+                        const float z0 = __uint_as_float(zr[2 * e]) + b1v[2 * e];
+                        const float z1 = __uint_as_float(zr[2 * e + 1]) + b1v[2 * e + 1];
                         __nv_bfloat162 hv = __float22bfloat162_rn(make_float2(z0, z1));
                         __nv_bfloat162 lv = __float22bfloat162_rn(
                             make_float2(z0 - __low2float(hv), z1 - __high2float(hv)));
@@ -483,6 +488,7 @@ static dsc_status launch_zfwd(const LowrankZArgs &a, const DeviceInfo &dev)
     constexpr int NB = CB * W, RB = CB * 2, XR = kM + W - 1, NBLK = (NB + 63) / 64;
     constexpr int NCW = CB / 8 < 4 ? CB / 8 : 4;
     Params p{};
+    p.b1 = a.b1;
     p.bias = a.bias;
     p.cu = a.cu;
     p.n_docs = a.n_docs;

@@ -121,20 +121,21 @@ dsc_status dsc_lowrank_fwd(const void *x, const void *z, const void *U, const fl
  *   projection on chip as well.  "Parameterization": the generator maps the
  *   layer input through D -> R -> W*D; "Placement": its first projection runs
  *   beside the Q/K/V projection, on the same input h.  Computes
- *     z[t, r]    = sum_i h[t, i] W1[r, i]
+ *     z[t, r]    = sum_i h[t, i] W1[r, i] + b1[r]
  *     w[t, d, k] = sum_r z[t, r] U[r, d*W+k] + bias[d*W+k]
  *   on the tensor cores (fp32 accumulation; z enters the second product
  *   rounded to bf16, as a stored activation would be) and never writes z or w
  *   to memory, then eq. 2 + eq. 3 with H = 1 on x.
  *   x [B,T,D], h [B,T,Dm], W1 [R,Dm] (row-major, as a linear layer's weight),
- *   U [R,D*W] in bf16, bias [D*W] fp32; writes y [B,T,D].  All caller-owned
- *   device memory.
+ *   U [R,D*W] in bf16; b1 [R] fp32 or NULL (no first bias; every transform of
+ *   the generator carries a bias, and b1 U can equally be folded into bias);
+ *   bias [D*W] fp32; writes y [B,T,D].  All caller-owned device memory.
  *   Requirements: those of dsc_lowrank_fwd, and Dm >= 1 with Dm % 8 == 0,
  *   R <= 128 (larger ranks -> DSC_ERR_UNSUPPORTED: compute z with a GEMM and
  *   call dsc_lowrank_fwd), B*T*Dm < 2^31.
  */
-dsc_status dsc_lowrank_zproj_fwd(const void *x, const void *h, const void *W1, const void *U, const float *bias,
-                                 void *y, int B, int T, int D, int Dm, int W, int R, dsc_dtype dt,
+dsc_status dsc_lowrank_zproj_fwd(const void *x, const void *h, const void *W1, const float *b1, const void *U,
+                                 const float *bias, void *y, int B, int T, int D, int Dm, int W, int R, dsc_dtype dt,
                                  const int32_t *cu_seqlens, int n_docs, cudaStream_t stream);
 
 /*

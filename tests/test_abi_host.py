@@ -124,17 +124,19 @@ def test_rejects_bad_arguments_before_any_launch(L):
     assert L.dsc_lowrank_bwd_workspace_bytes(1, 8, 16384, 4, 64) > 8 << 20
     assert L.dsc_lowrank_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 8, 16384, 4, 64, bf16, None, 0, None) == 1
     # the low-rank forward with z from the layer input: its own limits (R <= 128, Dm % 8 == 0) and pointers
-    zp = L.dsc_lowrank_zproj_fwd
-    assert zp(p, p, p, p, p, p, 1, 8, 64, 64, 4, 64, f32, None, 0, None) == 2
-    assert zp(p, p, p, p, p, p, 1, 8, 64, 64, 4, 136, bf16, None, 0, None) == 2
-    assert zp(p, p, p, p, p, p, 1, 8, 64, 60, 4, 64, bf16, None, 0, None) == 2
-    assert zp(p, p, p, p, p, p, 1, 8, 64, 0, 4, 64, bf16, None, 0, None) == 1
-    assert zp(p, None, p, p, p, p, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 1
-    assert zp(p, p, None, p, p, p, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 1
-    assert zp(p, p, p, p, p, None, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 1
-    assert zp(p, p, p, p, p, p, 1, 8, 64, 64, 9, 64, bf16, None, 0, None) == 1
-    assert zp(p, p, ctypes.c_void_p(0x10008), p, p, p, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 2  # W1 unaligned
-    assert zp(p, p, p, p, p, p, 1 << 16, 1 << 10, 64, 64, 4, 64, bf16, None, 0, None) == 1  # B*T*Dm >= 2^31
+    def zp(x, h, W1, b1, U, bias, y, *rest):
+        return L.dsc_lowrank_zproj_fwd(x, h, W1, b1, U, bias, y, *rest)
+    assert zp(p, p, p, None, p, p, p, 1, 8, 64, 64, 4, 64, f32, None, 0, None) == 2
+    assert zp(p, p, p, None, p, p, p, 1, 8, 64, 64, 4, 136, bf16, None, 0, None) == 2
+    assert zp(p, p, p, p, p, p, p, 1, 8, 64, 60, 4, 64, bf16, None, 0, None) == 2
+    assert zp(p, p, p, None, p, p, p, 1, 8, 64, 0, 4, 64, bf16, None, 0, None) == 1
+    assert zp(p, None, p, None, p, p, p, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 1
+    assert zp(p, p, None, None, p, p, p, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 1
+    assert zp(p, p, p, None, p, p, None, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 1
+    assert zp(p, p, p, None, p, p, p, 1, 8, 64, 64, 9, 64, bf16, None, 0, None) == 1
+    assert zp(p, p, ctypes.c_void_p(0x10008), None, p, p, p, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 2  # W1
+    assert zp(p, p, p, ctypes.c_void_p(0x10002), p, p, p, 1, 8, 64, 64, 4, 64, bf16, None, 0, None) == 1  # b1 unaligned
+    assert zp(p, p, p, None, p, p, p, 1 << 16, 1 << 10, 64, 64, 4, 64, bf16, None, 0, None) == 1  # B*T*Dm >= 2^31
     # the projection: H must divide D and be 1, 2, 4 or a multiple of 8; Dm % 8
     assert L.dsc_proj_fwd(p, p, p, None, p, 1, 8, 64, 64, 4, 12, bf16, None, 0, None) == 1
     assert L.dsc_proj_fwd(p, p, p, None, p, 1, 8, 64, 48, 4, 12, bf16, None, 0, None) == 2

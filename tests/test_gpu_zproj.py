@@ -1,6 +1,6 @@
 """GPU parity of the low-rank forward with the generator's first projection on chip (dsc_lowrank_zproj_fwd)
 against the fp64 oracle (oracle.lowrank_zproj_fwd), through the C ABI, on identical seeded inputs: the code
-z = h W1^T and the filter z U + bias are formed on the tensor cores and never stored; y is compared element by
+z = h W1^T + b1 and the filter z U + bias are formed on the tensor cores and never stored; y is compared element by
 element at the bf16 bound.  The kernel carries z into the second product as an exact pair of bf16 halves
 (about 16 significant bits); the oracle keeps it in fp64."""
 import zlib
@@ -57,9 +57,12 @@ def test_zproj_small(dsc, oracle_mod, case):
                              doc_min=1, doc_max=60)
     d = inputs.make(wl)
     g = _dev(d)
-    y = dsc.dsc_lowrank_zproj_fwd(g["x"], g["h"], g["W1"], g["U"], g["bias"], cu_seqlens=g["cu_seqlens"])
+    with_b1 = R != 16  # one rank without the first bias
+    y = dsc.dsc_lowrank_zproj_fwd(g["x"], g["h"], g["W1"], g["U"], g["bias"], b1=g["b1"] if with_b1 else None,
+                                  cu_seqlens=g["cu_seqlens"])
     assert dsc.dsc_sync_status() == dsc.DSC_OK
-    ry = oracle_mod.lowrank_zproj_fwd(d["x"], d["h"], d["W1"], d["U"], d["bias"], W, cu_seqlens=d["cu_seqlens"])
+    ry = oracle_mod.lowrank_zproj_fwd(d["x"], d["h"], d["W1"], d["U"], d["bias"], W, cu_seqlens=d["cu_seqlens"],
+                                      b1=d["b1"] if with_b1 else None)
     assert_close(y.reshape(B * T, D), ry, "bf16", "y")
 
 
@@ -69,7 +72,7 @@ def test_zproj_full_size_sampled(dsc, oracle_mod):
     wl = inputs.WORKLOADS[9]
     d = inputs.make(wl)
     g = _dev(d)
-    y = dsc.dsc_lowrank_zproj_fwd(g["x"], g["h"], g["W1"], g["U"], g["bias"], cu_seqlens=g["cu_seqlens"])
+    y = dsc.dsc_lowrank_zproj_fwd(g["x"], g["h"], g["W1"], g["U"], g["bias"], b1=g["b1"], cu_seqlens=g["cu_seqlens"])
     assert dsc.dsc_sync_status() == dsc.DSC_OK
     BT = wl.B * wl.T
     y = y.reshape(BT, wl.D)
@@ -78,19 +81,19 @@ def test_zproj_full_size_sampled(dsc, oracle_mod):
     for r0 in starts:
         r1 = min(r0 + 4, BT)
         ry = oracle_mod.lowrank_zproj_fwd(d["x"], d["h"], d["W1"], d["U"], d["bias"], wl.W,
-                                          cu_seqlens=d["cu_seqlens"], rows=(r0, r1))
+                                          cu_seqlens=d["cu_seqlens"], rows=(r0, r1), b1=d["b1"])
         assert_close(y[r0:r1], ry, "bf16", f"y rows {r0}:{r1}")
     assert torch.isfinite(y).all()
 
 
 def test_zproj_equals_unfused_path(dsc):
-    """Against the unfused path built from the library's own pieces: z = h W1^T by torch's matmul, rounded to
+    """Against the unfused path built from the library's own pieces: z = h W1^T + b1 by torch's matmul, rounded to
     bf16 as a caller would store it, then dsc_lowrank_fwd.  The fused call keeps z to about 16 bits, so the two
     differ by that rounding of z: a few thousandths of the largest |y|."""
     wl = inputs.custom_zproj(2, 400, 512, 256, 4, 64, seed_id=760, packed=True, doc_min=5, doc_max=90)
     g = _dev(inputs.make(wl))
-    y = dsc.dsc_lowrank_zproj_fwd(g["x"], g["h"], g["W1"], g["U"], g["bias"], cu_seqlens=g["cu_seqlens"])
-    z = (g["h"].float() @ g["W1"].float().T).bfloat16()
+    y = dsc.dsc_lowrank_zproj_fwd(g["x"], g["h"], g["W1"], g["U"], g["bias"], b1=g["b1"], cu_seqlens=g["cu_seqlens"])
+    z = (g["h"].float() @ g["W1"].float().T + g["b1"]).bfloat16()
     y2 = dsc.dsc_lowrank_fwd(g["x"], z, g["U"], g["bias"], cu_seqlens=g["cu_seqlens"])
     assert dsc.dsc_sync_status() == dsc.DSC_OK
     diff = (y.float() - y2.float()).abs().max().item()
