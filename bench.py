@@ -79,7 +79,7 @@ DENSE_BWD_SRC = ["dsc_dense_bwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 DENSE_FWD_SRC = ["dsc_dense_fwd.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 LOWRANK_BWD_SRC = ["dsc_lowrank_bwd.cu", "dsc_lowrank_bwd_du.cu", "dsc_lowrank_common.cuh", "dsc_tcgen05.cuh",
                    "dsc_device.cuh"]
-LOWRANK_FWD_SRC = ["dsc_lowrank_fwd.cu", "dsc_lowrank_common.cuh", "dsc_tcgen05.cuh", "dsc_device.cuh"]
+LOWRANK_FWD_SRC = ["dsc_lowrank_fwd.cu", "dsc_lowrank_epi.cuh", "dsc_lowrank_common.cuh", "dsc_tcgen05.cuh", "dsc_device.cuh"]
 STATIC_SRC = ["dsc_static.cu", "dsc_dense_common.cuh", "dsc_device.cuh"]
 # (kernel name in the ncu launch list, source files) per workload kind and direction
 KERNELS = {("dense", "bwd"): ("dense_bwd_tma", DENSE_BWD_SRC), ("dense", "fwd"): ("dense_fwd_tma", DENSE_FWD_SRC),

@@ -23,6 +23,7 @@
 // pairs feed packed fp32x2 math straight from TMEM registers.
 #include "dsc_internal.h"
 #include "dsc_lowrank_common.cuh"  // swizzled tile offsets (swzt), swizzle_for; tcgen05 wrappers
+#include "dsc_lowrank_epi.cuh"    // y of a token's 8-channel group from its filter row and x window
 
 namespace dsc {
 
@@ -302,53 +303,7 @@ __global__ void __launch_bounds__(lrf::kThreads, 1)
 #pragma unroll
             for (int gi = 0; gi < GPW; ++gi) {
                 const int g = h * GPW + gi;  // 8-channel group
-                uint32_t acc[8 * W];         // acc[c*W + k]: tap k of channel g*8 + c
-                tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
-                uint32_t xw[W][4];           // x~ rows row-k of the group's 8 channels, bf16 pairs
-#pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swzt<RB>(row + (W - 1) - k, g));
-                    xw[k][0] = raw.x;
-                    xw[k][1] = raw.y;
-                    xw[k][2] = raw.z;
-                    xw[k][3] = raw.w;
-                }
-                if (!full_taps) {  // x~ is zero before the document start (warp-uniform branch)
-#pragma unroll
-                    for (int k = 1; k < W; ++k)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) xw[k][e] = k < nv ? xw[k][e] : 0u;
-                }
-                tmem_ld_wait();
-                float2 out[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float y2[2];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {  // channel c = 2e + h2
-                        const int c = 2 * e + h2;
-                        auto xv = [&](int k) {
-                            const uint32_t w2 = xw[k][e];
-                            return __uint_as_float(h2 ? (w2 & 0xffff0000u) : (w2 << 16));
-                        };
-                        // residual + sum_k acc_k * x~_k, taps paired for packed fp32x2 arithmetic
-                        float2 sum = make_float2(xv(0), 0.f);
-#pragma unroll
-                        for (int k = 0; k + 1 < W; k += 2)
-                            sum = fma2(make_float2(__uint_as_float(acc[c * W + k]), __uint_as_float(acc[c * W + k + 1])),
-                                       make_float2(xv(k), xv(k + 1)), sum);
-                        if constexpr (W % 2 == 1) sum.x = fmaf(__uint_as_float(acc[c * W + W - 1]), xv(W - 1), sum.x);
-                        y2[h2] = sum.x + sum.y;
-                    }
-                    out[e] = make_float2(y2[0], y2[1]);
-                }
-                uint4 o;
-                __nv_bfloat162 h0 = __float22bfloat162_rn(out[0]), h1 = __float22bfloat162_rn(out[1]);
-                __nv_bfloat162 h2 = __float22bfloat162_rn(out[2]), h3 = __float22bfloat162_rn(out[3]);
-                o.x = *reinterpret_cast<uint32_t *>(&h0);
-                o.y = *reinterpret_cast<uint32_t *>(&h1);
-                o.z = *reinterpret_cast<uint32_t *>(&h2);
-                o.w = *reinterpret_cast<uint32_t *>(&h3);
+                const uint4 o = lr_group_y<W, RB>(trow + g * 8 * W, xs, row, g, full_taps, nv);
                 if (!ys_free) {
                     if (lane == 0) tma_store_wait_read<1>();
                     __syncwarp();

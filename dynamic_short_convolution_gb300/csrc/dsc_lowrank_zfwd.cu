@@ -36,6 +36,7 @@
 
 #include "dsc_internal.h"
 #include "dsc_lowrank_common.cuh"
+#include "dsc_lowrank_epi.cuh"
 
 namespace dsc {
 
@@ -400,47 +401,7 @@ __global__ void __launch_bounds__(lrz::kThreads, 1)
 #pragma unroll
             for (int gi = 0; gi < GPW; ++gi) {
                 const int g = h * GPW + gi;  // 8-channel group
-                uint32_t acc[8 * W];         // acc[c*W + k]: tap k of channel g*8 + c
-                tmem_ld_cols<8 * W>(trow + g * 8 * W, acc);
-                uint32_t xw[W][4];           // x~ rows row-k of the group's 8 channels, bf16 pairs
-#pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(xs + swzt<RB>(row + (W - 1) - k, g));
-                    xw[k][0] = raw.x;
-                    xw[k][1] = raw.y;
-                    xw[k][2] = raw.z;
-                    xw[k][3] = raw.w;
-                }
-                if (!full_taps) {  // x~ is zero before the document start (warp-uniform branch)
-#pragma unroll
-                    for (int k = 1; k < W; ++k)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) xw[k][e] = k < nv ? xw[k][e] : 0u;
-                }
-                tmem_ld_wait();
-                uint32_t packed[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float y2[2];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {  // channel c = 2e + h2
-                        const int c = 2 * e + h2;
-                        auto xv = [&](int k) {
-                            const uint32_t w2 = xw[k][e];
-                            return __uint_as_float(h2 ? (w2 & 0xffff0000u) : (w2 << 16));
-                        };
-                        float2 sum = make_float2(xv(0), 0.f);
-#pragma unroll
-                        for (int k = 0; k + 1 < W; k += 2)
-                            sum = fma2(make_float2(__uint_as_float(acc[c * W + k]), __uint_as_float(acc[c * W + k + 1])),
-                                       make_float2(xv(k), xv(k + 1)), sum);
-                        if constexpr (W % 2 == 1) sum.x = fmaf(__uint_as_float(acc[c * W + W - 1]), xv(W - 1), sum.x);
-                        y2[h2] = sum.x + sum.y;
-                    }
-                    __nv_bfloat162 hv = __float22bfloat162_rn(make_float2(y2[0], y2[1]));
-                    packed[e] = *reinterpret_cast<uint32_t *>(&hv);
-                }
-                o[gi] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                o[gi] = lr_group_y<W, RB>(trow + g * 8 * W, xs, row, g, full_taps, nv);
             }
             // accumulator and x tile read: hand them back; stage and store this warp's y sub-tile (the staging
             // tile is free once the store issued a unit ago has read it)
