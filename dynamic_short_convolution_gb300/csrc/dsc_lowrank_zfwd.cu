@@ -18,20 +18,21 @@
 // CTA takes a contiguous run of units, which covers one or two token tiles,
 // and computes z once for each tile it touches.  (Whole tiles per CTA read h
 // once but leave SMs idle when there are fewer tiles than SMs: measured
-// slower.)  One ring of shared-memory slots carries two
-// kinds of items in the order the CTA needs them: "z items" (two 64-wide K
-// chunks of the h tile and of W1) when a token tile starts, and one "unit
-// item" per unit (the block's U rows with the bias as two extra rows, and the
-// x tile with its (W-1)-token causal halo).
+// slower.)  One ring of shared-memory slots carries two kinds of items in the
+// order the CTA needs them: "z items" (two 64-wide K chunks of the h tile and
+// of W1) when a token tile starts, and one "unit item" per unit (the block's
+// U rows with the bias as 16 extra rows, and the x tile with its (W-1)-token
+// causal halo).
 //   warp 0      producer: TMA loads of every item; writes the bias rows of
-//               each unit item (bf16 hi and lo, 14 zero rows after them)
+//               each unit item (bf16 hi and lo, 14 zero rows after them) from
+//               the bias it loaded during the previous item
 //   warp 1      TMEM owner; lane 0 issues the z MMAs (M=128, N=R, K=16) into
 //               the accumulator the tile's first unit will use, then per unit
 //               the filter MMAs [z_hi | z_lo | 1] . [U ; U ; b_hi + b_lo]
-//   warps 2..17 epilogue: at a token tile's start they read z from TMEM and
-//               write it as bf16 into the z tile; per unit, as the low-rank
-//               forward: the accumulator row of a token times its x window,
-//               plus the residual, staged and TMA-stored per warp
+//   warps 2..17 epilogue: at a token tile's start they read z from TMEM, add
+//               b1 and write it as the bf16 hi + lo z tile; per unit, as the
+//               low-rank forward: the accumulator row of a token times its x
+//               window, plus the residual, staged and TMA-stored per warp
 #include <type_traits>
 
 #include "dsc_internal.h"
